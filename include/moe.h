@@ -1,0 +1,156 @@
+/*
+ * moe.h — C ABI of libmoe.so: one top-k Mixture-of-Experts layer on one GB300
+ * (sm_103a).
+ *
+ * The layer. Every decoder layer of Muse Spark is a Mixture-of-Experts layer
+ * in which each token picks 8 of 256 experts ("How SGLang-TorchTPU
+ * accelerated an 816B-parameter MoE on TPU v7", section "Introduction");
+ * per-expert outputs are combined after the experts run ("TensorSharp Muse
+ * Spark benchmark", section "Performance"); partial sums of expert outputs
+ * are kept in fp32 because bf16 partial sums cost quality (same page, section
+ * "Answer quality"). The pages leave the gate and FFN open; this library
+ * computes, per token t with bf16 input x[t, 0:d]:
+ *
+ *   logit[e] = sum_c x[c] * Wr[e, c]  (fp32 accumulate) + bias[e]
+ *   p        = softmax(logit) over all E experts (fp32)
+ *   ids[0:k] = the k largest p, ties to the lower expert id, by descending p
+ *   w[j]     = p[ids[j]] / sum_j' p[ids[j']]
+ *   h_j      = silu(Wg[ids[j]] x) * (Wu[ids[j]] x)
+ *   y        = sum_j w[j] * (Wd[ids[j]] h_j)   (fp32, j ascending) -> bf16
+ *
+ * Conventions for every call:
+ *  - Pointers named *_host are host memory; every other pointer is device
+ *    memory owned by the caller, 16-byte aligned, and must stay valid for as
+ *    long as the layer or the enqueued work uses it. The library allocates no
+ *    device memory: scratch lives in the caller's workspace.
+ *  - `stream` is a cudaStream_t passed as void* (NULL: the legacy default
+ *    stream). All device work is enqueued on it, in order; calls return
+ *    without waiting for the GPU unless stated otherwise.
+ *  - bf16 tensors are raw bf16 bits, row-major, innermost index last.
+ *  - Argument errors are detected on the host before any work is enqueued
+ *    (MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED); launch failures return
+ *    MOE_ERR_CUDA; conditions detected by a kernel (a bounded wait that ran
+ *    out, an index out of range) set an error word in the workspace that
+ *    moe_get_device_status() reports.
+ *  - A layer object is not thread-safe; distinct layers may be used from
+ *    distinct threads. Two calls on one layer must not overlap on the GPU
+ *    (they share the workspace): issue them on one stream.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1,  /* null pointer, misaligned pointer, T out of range */
+    MOE_ERR_UNSUPPORTED = 2,  /* shape or format this library does not implement */
+    MOE_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE = 4,       /* a kernel flagged an out-of-range index */
+    MOE_ERR_TIMEOUT = 5       /* a kernel's bounded wait ran out */
+} moe_status;
+
+/* Expert weight format. NVFP4 ("How SGLang-TorchTPU accelerated an
+ * 816B-parameter MoE on TPU v7", section "Results and interpretation", runs
+ * experts as NVFP4 weights): 16-element blocks along the contraction index,
+ * each element an E2M1 code, each block one E4M3 scale, each tensor (one
+ * matrix of one expert) one fp32 scale: w = e2m1 * e4m3 * s_tensor. */
+typedef enum { MOE_W_BF16 = 0, MOE_W_NVFP4 = 1 } moe_wfmt;
+
+typedef struct moe_layer moe_layer;
+
+/* Layer description. Shapes: E experts, hidden size d, expert width I, k
+ * experts per token, at most max_tokens tokens per call.
+ * Supported: 1 <= k <= 8, k <= E <= 256, d and I multiples of 64, d <= 8192,
+ * I <= 4096, 1 <= max_tokens <= 65536. */
+typedef struct {
+    int d, E, top_k, I, max_tokens;
+    moe_wfmt fmt;
+    const void *w_router;     /* [E, d] bf16 */
+    const float *router_bias; /* [E] fp32, or NULL for no bias */
+    /* MOE_W_BF16 experts (NULL otherwise) */
+    const void *w_gate;       /* [E, I, d] bf16 */
+    const void *w_up;         /* [E, I, d] bf16 */
+    const void *w_down;       /* [E, d, I] bf16 */
+    /* MOE_W_NVFP4 experts (NULL otherwise). Two E2M1 codes per byte, the low
+     * nibble holding the lower contraction index; E4M3 scales one per 16. */
+    const uint8_t *q_gate, *q_up; /* [E, I, d/2] */
+    const uint8_t *q_down;        /* [E, d, I/2] */
+    const uint8_t *s_gate, *s_up; /* [E, I, d/16] */
+    const uint8_t *s_down;        /* [E, d, I/16] */
+    const float *g_gate, *g_up, *g_down; /* [E] per-tensor fp32 scales */
+} moe_layer_desc;
+
+/* Bytes of device workspace the layer needs (for max_tokens). No GPU work. */
+moe_status moe_workspace_size(const moe_layer_desc *desc, size_t *bytes);
+
+/* Create a layer over caller-owned weights and workspace (ws_bytes at least
+ * moe_workspace_size; 256-byte aligned). Zeroes the workspace's control words
+ * with a synchronous cudaMemset on the current device; *out receives a
+ * host-side handle freed by moe_layer_destroy. */
+moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t ws_bytes,
+                            moe_layer **out);
+
+/* Routing and token permutation only (router, softmax, top-k, renormalise,
+ * then the permutation). x [T, d] bf16. Outputs (device):
+ *   ids [T, k] int32 (descending weight), w [T, k] fp32 (sums to 1 per token),
+ *   counts [E] int32, offsets [E+1] int32 (exclusive prefix sum of counts),
+ *   perm [T*k] int32: perm[offsets[e] + r] = the r-th smallest token id routed
+ *   to expert e, pos [T, k] int32: the row of (t, j) in that order.
+ * Any output pointer may be NULL to skip it. 1 <= T <= max_tokens. */
+moe_status moe_route(moe_layer *layer, const void *x, int T, int32_t *ids, float *w,
+                     int32_t *counts, int32_t *offsets, int32_t *perm, int32_t *pos,
+                     void *stream);
+
+/* Layer forward: out [T, d] bf16 = MoE(x). out must not alias x. */
+moe_status moe_forward(moe_layer *layer, const void *x, void *out, int T, void *stream);
+
+/* out = bf16(res + MoE(x)) with the residual added in fp32. out may alias res
+ * but not x. Used between stacked layers (pre-norm residual block). */
+moe_status moe_forward_residual(moe_layer *layer, const void *x, const void *res, void *out,
+                                int T, void *stream);
+
+/* End-to-end forward from host memory: copies x_host [T, d] bf16 into the
+ * workspace, runs moe_forward, copies the result to out_host [T, d] bf16 and
+ * waits for the stream. Page-locked host buffers give asynchronous copies. */
+moe_status moe_forward_host(moe_layer *layer, const void *x_host, void *out_host, int T,
+                            void *stream);
+
+/* Expert outputs of the last forward on this layer, before the weighted sum:
+ * Y [T*k, d] fp32, row pos[t, j] holding expert ids[t, j] applied to token t
+ * (pos from moe_route on the same x). For parity checks of every slot. */
+moe_status moe_debug_expert_outputs(moe_layer *layer, float *Y, int T, void *stream);
+
+/* Row-wise RMSNorm without a learned scale: out = x / sqrt(mean(x^2) + eps),
+ * x and out [T, d] bf16 (out may alias x), fp32 arithmetic. */
+moe_status moe_rmsnorm(const void *x, void *out, int T, int d, float eps, void *stream);
+
+/* NVFP4 quantiser for n tensors of shape [rows, K] (bf16, contiguous):
+ *   s_t = amax|W| / (6*448) (1 for an all-zero tensor),
+ *   block scale = E4M3((amax_block / 6) / s_t), code = E2M1(w / (scale * s_t)),
+ * round-to-nearest-even, saturating. Outputs q [n, rows, K/2], s [n, rows, K/16],
+ * g [n] fp32 (g is also used as the amax accumulator). K multiple of 32. */
+moe_status moe_quantize_nvfp4(const void *W, int n, int rows, int K, uint8_t *q, uint8_t *s,
+                              float *g, void *stream);
+
+/* Waits for `stream`, then reads and clears the layer's device error word:
+ * MOE_OK, MOE_ERR_DEVICE or MOE_ERR_TIMEOUT. */
+moe_status moe_get_device_status(moe_layer *layer, void *stream);
+
+/* Number of kernel launches the last forward/route on this layer enqueued. */
+int moe_last_launch_count(const moe_layer *layer);
+
+moe_status moe_layer_destroy(moe_layer *layer);
+
+const char *moe_status_string(moe_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */
