@@ -145,6 +145,16 @@ moe_status moe_get_device_status(moe_layer *layer, void *stream);
 /* Number of kernel launches the last forward/route on this layer enqueued. */
 int moe_last_launch_count(const moe_layer *layer);
 
+/* Per-kernel timing for measurement. After moe_profile_begin(layer, n), each
+ * of the next n forwards on the layer also records a CUDA event on its stream
+ * before each of its kernels and one after the last (host-side event objects;
+ * no device memory). moe_profile_end waits for those events and writes
+ * ms[f * max_kernels + i] = duration of kernel i of recorded forward f, and
+ * the counts, then stops recording. */
+moe_status moe_profile_begin(moe_layer *layer, int max_forwards);
+moe_status moe_profile_end(moe_layer *layer, float *ms_host, int max_kernels, int *n_forwards,
+                           int *n_kernels);
+
 moe_status moe_layer_destroy(moe_layer *layer);
 
 const char *moe_status_string(moe_status s);

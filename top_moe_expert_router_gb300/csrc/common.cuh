@@ -1,0 +1,244 @@
+// common.cuh — shared device helpers of libmoe: inline PTX for mbarriers and
+// bulk (TMA) copies, bounded waits, bf16 unpacking, and the workspace layout.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// Error word (first word of the workspace). Kernels OR these bits in; the host
+// reads and clears them in moe_get_device_status().
+// ---------------------------------------------------------------------------
+enum : uint32_t { ERRBIT_TIMEOUT = 1u, ERRBIT_RANGE = 2u };
+
+// A bounded wait gives up after this many nanoseconds of global time.
+constexpr unsigned long long kWaitLimitNs = 1500000000ull;  // 1.5 s
+
+// ---------------------------------------------------------------------------
+// Workspace layout. All regions 256-byte aligned; sizes depend on the layer
+// shape and max_tokens only.
+// ---------------------------------------------------------------------------
+struct Control {
+    uint32_t err;            // error bits
+    uint32_t route_done;     // arrival counter of the router's CTAs (reset by the last)
+    int32_t n_uniq;          // number of experts with at least one token
+    int32_t n_tiles_gu;      // prefill: gate/up tiles
+    int32_t n_tiles_dn;      // prefill: down tiles
+    int32_t pad[59];
+};
+
+struct Workspace {
+    Control *ctrl;
+    float *logits;      // [max_T, E]
+    int32_t *ids;       // [max_T, k]
+    float *w;           // [max_T, k]
+    int32_t *counts;    // [E]
+    int32_t *offsets;   // [E+1]
+    int32_t *uniq;      // [E] experts with tokens, ascending
+    int32_t *tile_off;  // [E+1] prefill: exclusive scan of 128-row tiles per expert
+    int32_t *perm;      // [max_T*k]
+    int32_t *pos;       // [max_T*k]
+    uint16_t *xbuf;     // [max_T, d] bf16 staging (host forward, rmsnorm)
+    uint16_t *obuf;     // [max_T, d] bf16 staging
+    float *h;           // [max_T*k, I] fp32 (decode) / bf16 (prefill)
+    float *Y;           // [max_T*k, d] fp32 expert outputs
+    uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill)
+    size_t bytes;
+};
+
+inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// Computes the layout; with base == nullptr only the size is meaningful.
+inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int max_T) {
+    Workspace ws{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        size_t o = off;
+        off = align_up(off + bytes, 256);
+        return base ? (void *)((char *)base + o) : nullptr;
+    };
+    size_t Tk = (size_t)max_T * k;
+    ws.ctrl = (Control *)take(sizeof(Control));
+    ws.logits = (float *)take(sizeof(float) * (size_t)max_T * E);
+    ws.ids = (int32_t *)take(sizeof(int32_t) * Tk);
+    ws.w = (float *)take(sizeof(float) * Tk);
+    ws.counts = (int32_t *)take(sizeof(int32_t) * E);
+    ws.offsets = (int32_t *)take(sizeof(int32_t) * (E + 1));
+    ws.uniq = (int32_t *)take(sizeof(int32_t) * E);
+    ws.tile_off = (int32_t *)take(sizeof(int32_t) * (E + 1));
+    ws.perm = (int32_t *)take(sizeof(int32_t) * Tk);
+    ws.pos = (int32_t *)take(sizeof(int32_t) * Tk);
+    ws.xbuf = (uint16_t *)take(sizeof(uint16_t) * (size_t)max_T * d);
+    ws.obuf = (uint16_t *)take(sizeof(uint16_t) * (size_t)max_T * d);
+    ws.h = (float *)take(sizeof(float) * Tk * I);
+    ws.Y = (float *)take(sizeof(float) * Tk * d);
+    ws.xperm = (uint16_t *)take(sizeof(uint16_t) * Tk * d);
+    ws.bytes = off;
+    return ws;
+}
+
+// ---------------------------------------------------------------------------
+// Device helpers
+// ---------------------------------------------------------------------------
+#ifdef __CUDACC__
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Waits until the phase of `bar` with the given parity has completed. Gives up
+// after kWaitLimitNs, sets ERRBIT_TIMEOUT in *err and returns false.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0 && global_ns() - t0 > kWaitLimitNs) {
+            atomicOr(err, ERRBIT_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// As mbar_wait, but also gives up (returning false) once *abort is set by
+// another warp of the CTA; a timeout sets *abort for the others.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t *bar, uint32_t parity, uint32_t *err,
+                                                   volatile int *abort) {
+    if (mbar_try_wait(bar, parity)) return true;
+    unsigned long long t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((it & 255u) == 0) {
+            if (*abort) return false;
+            if (global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(err, ERRBIT_TIMEOUT);
+                *abort = 1;
+                return false;
+            }
+        }
+    }
+}
+
+// Bulk (non-tensor) TMA copy global -> shared, completing on `bar` with a byte count.
+// dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes, uint64_t *bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Named barrier over `nthreads` threads (a multiple of 32), id 1..15.
+__device__ __forceinline__ void named_bar(uint32_t id, uint32_t nthreads) {
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+__device__ __forceinline__ uint16_t f32_to_bf16_rn(float f) {
+    uint32_t u = __float_as_uint(f);
+    if ((u & 0x7F800000u) == 0x7F800000u && (u & 0x007FFFFFu)) return (uint16_t)((u >> 16) | 0x40u);
+    u += 0x7FFFu + ((u >> 16) & 1u);
+    return (uint16_t)(u >> 16);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
+
+#endif  // __CUDACC__
+
+// ---------------------------------------------------------------------------
+// Launchers (defined in the .cu files), all asynchronous on `st`.
+// ---------------------------------------------------------------------------
+struct LayerDev {
+    int d, E, k, I, max_T;
+    moe_wfmt fmt;
+    const uint16_t *wr;
+    const float *bias;
+    const uint16_t *wg, *wu, *wd;
+    const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
+    const float *gg, *gu, *gd;
+    int num_sms;
+};
+
+// route.cu
+cudaError_t launch_route_small(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
+                               int *launches);
+// decode.cu
+cudaError_t launch_decode_gateup(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+cudaError_t launch_decode_down(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+// misc.cu
+cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
+                           cudaStream_t st);
+cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int d, float eps, cudaStream_t st);
+cudaError_t launch_quantize_nvfp4(const uint16_t *W, int n, int rows, int K, uint8_t *q, uint8_t *s, float *g,
+                                  cudaStream_t st);
+cudaError_t launch_gather_rows(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+// prefill.cu
+cudaError_t launch_router_gemm(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
+                                   int *launches);
+
+}  // namespace moe

@@ -1,0 +1,203 @@
+// misc.cu — weighted combine, RMSNorm, NVFP4 quantiser and row gather.
+//
+// The combine sums the k expert outputs of a token in fp32, slot order fixed
+// (j ascending): per-expert outputs are combined after the experts run, and
+// bf16 partial sums of expert outputs cost quality ("TensorSharp Muse Spark
+// benchmark", sections "Performance" and "Answer quality").
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// combine: out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] )
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ Y, const float *__restrict__ w,
+                                                      const int32_t *__restrict__ pos,
+                                                      const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
+                                                      int T, int d, int k, uint32_t *err, int rows) {
+    const int t = blockIdx.y;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (c >= d) return;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = 0; j < k; ++j) {
+        const float wj = w[(size_t)t * k + j];
+        const int r = pos[(size_t)t * k + j];
+        if ((unsigned)r >= (unsigned)rows) {
+            atomicOr(err, ERRBIT_RANGE);
+            continue;
+        }
+        const float4 y = __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)r * d + c));
+        acc.x = fmaf(wj, y.x, acc.x);
+        acc.y = fmaf(wj, y.y, acc.y);
+        acc.z = fmaf(wj, y.z, acc.z);
+        acc.w = fmaf(wj, y.w, acc.w);
+    }
+    if (res) {
+        const uint2 rv = *reinterpret_cast<const uint2 *>(res + (size_t)t * d + c);
+        acc.x += bf16lo(rv.x);
+        acc.y += bf16hi(rv.x);
+        acc.z += bf16lo(rv.y);
+        acc.w += bf16hi(rv.y);
+    }
+    uint2 o;
+    o.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
+    o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
+    *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = o;
+}
+
+cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
+                           cudaStream_t st) {
+    dim3 grid((L.d / 4 + 255) / 256, T);
+    combine_kernel<<<grid, 256, 0, st>>>(ws.Y, ws.w, ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm without learned scale: out = x / sqrt(mean(x^2) + eps)
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const uint16_t *__restrict__ x, uint16_t *__restrict__ out,
+                                                      int d, float eps) {
+    __shared__ float part[8];
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint16_t *xr = x + (size_t)t * d;
+    float ss = 0.f;
+    for (int c = tid * 8; c < d; c += 256 * 8) {
+        uint4 v = *reinterpret_cast<const uint4 *>(xr + c);
+        uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            float lo = bf16lo(a[i]), hi = bf16hi(a[i]);
+            ss = fmaf(lo, lo, ss);
+            ss = fmaf(hi, hi, ss);
+        }
+    }
+    ss = warp_sum(ss);
+    if ((tid & 31) == 0) part[tid >> 5] = ss;
+    __syncthreads();
+    float tot = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) tot += part[i];
+    const float r = 1.0f / sqrtf(tot / (float)d + eps);
+    for (int c = tid * 8; c < d; c += 256 * 8) {
+        uint4 v = *reinterpret_cast<const uint4 *>(xr + c);
+        uint32_t a[4] = {v.x, v.y, v.z, v.w}, o[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            o[i] = (uint32_t)f32_to_bf16_rn(bf16lo(a[i]) * r) | ((uint32_t)f32_to_bf16_rn(bf16hi(a[i]) * r) << 16);
+        *reinterpret_cast<uint4 *>(out + (size_t)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int d, float eps, cudaStream_t st) {
+    rmsnorm_kernel<<<T, 256, 0, st>>>(x, out, d, eps);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// NVFP4 quantiser. Tensor scale s_t = amax / (6 * 448); block scale
+// E4M3((amax_block / 6) / s_t); codes E2M1(w / (scale * s_t)); fp32 throughout,
+// round to nearest even with saturation (the hardware conversions), the sign
+// of a code always that of w.
+// ---------------------------------------------------------------------------
+__global__ void amax_kernel(const uint16_t *__restrict__ W, size_t per_tensor, float *amax_bits) {
+    const int n = blockIdx.y;
+    const uint16_t *src = W + (size_t)n * per_tensor;
+    float m = 0.f;
+    for (size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < per_tensor;
+         i += (size_t)gridDim.x * blockDim.x * 8) {
+        uint4 v = *reinterpret_cast<const uint4 *>(src + i);
+        uint32_t a[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(a[j])), fabsf(bf16hi(a[j]))));
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+    // non-negative floats order like their bit patterns
+    if ((threadIdx.x & 31) == 0) atomicMax(reinterpret_cast<unsigned int *>(amax_bits + n), __float_as_uint(m));
+}
+
+__device__ __forceinline__ float tensor_scale_from_amax(float amax) { return amax > 0.f ? amax / 2688.0f : 1.0f; }
+
+__global__ void quantize_kernel(const uint16_t *__restrict__ W, size_t per_tensor, int K, const float *amax,
+                                uint8_t *__restrict__ q, uint8_t *__restrict__ s) {
+    const int n = blockIdx.y;
+    const size_t nblk = per_tensor / 16;
+    const float st = tensor_scale_from_amax(amax[n]);
+    for (size_t b = (size_t)blockIdx.x * blockDim.x + threadIdx.x; b < nblk; b += (size_t)gridDim.x * blockDim.x) {
+        const uint4 *src = reinterpret_cast<const uint4 *>(W + (size_t)n * per_tensor + b * 16);
+        uint4 v0 = src[0], v1 = src[1];
+        uint32_t a[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+        float wv[16];
+        float bmax = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            wv[2 * j] = bf16lo(a[j]);
+            wv[2 * j + 1] = bf16hi(a[j]);
+            bmax = fmaxf(bmax, fmaxf(fabsf(wv[2 * j]), fabsf(wv[2 * j + 1])));
+        }
+        const float sbf = __fdiv_rn(__fdiv_rn(bmax, 6.0f), st);
+        const __nv_fp8_storage_t sc = __nv_cvt_float_to_fp8(sbf, __NV_SATFINITE, __NV_E4M3);
+        __half_raw hr = __nv_cvt_fp8_to_halfraw(sc, __NV_E4M3);
+        const float scale = __fmul_rn(__half2float(*reinterpret_cast<__half *>(&hr)), st);
+        uint32_t packed[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            uint32_t code = 0u;
+            if (scale != 0.f) {
+                const float r = __fdiv_rn(wv[j], scale);
+                code = (uint32_t)__nv_cvt_float_to_fp4(fabsf(r), __NV_E2M1, cudaRoundNearest) & 0x7u;
+                code |= (__float_as_uint(wv[j]) >> 31) << 3;
+            }
+            packed[j >> 3] |= code << (4 * (j & 7));
+        }
+        *reinterpret_cast<uint2 *>(q + (size_t)n * (per_tensor / 2) + b * 8) = make_uint2(packed[0], packed[1]);
+        s[(size_t)n * nblk + b] = (uint8_t)sc;
+    }
+}
+
+__global__ void finalize_scale_kernel(float *g, int n) {
+    int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) g[i] = tensor_scale_from_amax(g[i]);
+}
+
+cudaError_t launch_quantize_nvfp4(const uint16_t *W, int n, int rows, int K, uint8_t *q, uint8_t *s, float *g,
+                                  cudaStream_t st) {
+    size_t per = (size_t)rows * K;
+    cudaError_t e = cudaMemsetAsync(g, 0, sizeof(float) * n, st);
+    if (e != cudaSuccess) return e;
+    int bx = (int)((per / 8 + 255) / 256);
+    if (bx > 1024) bx = 1024;
+    amax_kernel<<<dim3(bx, n), 256, 0, st>>>(W, per, g);
+    int qx = (int)((per / 16 + 255) / 256);
+    if (qx > 2048) qx = 2048;
+    quantize_kernel<<<dim3(qx, n), 256, 0, st>>>(W, per, K, g, q, s);
+    finalize_scale_kernel<<<(n + 255) / 256, 256, 0, st>>>(g, n);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// gather: xperm[r, :] = x[perm[r], :] (prefill operand rows in expert order)
+// ---------------------------------------------------------------------------
+__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
+                                   uint16_t *__restrict__ xp, int rows, int d, int T, uint32_t *err) {
+    const int r = blockIdx.x;
+    const int t = perm[r];
+    if ((unsigned)t >= (unsigned)T) {
+        if (threadIdx.x == 0) atomicOr(err, ERRBIT_RANGE);
+        return;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * d);
+    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+}
+
+cudaError_t launch_gather_rows(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st) {
+    gather_rows_kernel<<<T * L.k, 256, 0, st>>>(x, ws.perm, ws.xperm, T * L.k, L.d, T, &ws.ctrl->err);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

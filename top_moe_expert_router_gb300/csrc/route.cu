@@ -1,0 +1,331 @@
+// route.cu — router (bf16 x . Wr^T with fp32 accumulation), fp32 softmax,
+// top-k with renormalisation, and the token permutation.
+//
+// Each token picks k of E experts (k = 8, E = 256 in "How SGLang-TorchTPU
+// accelerated an 816B-parameter MoE on TPU v7", section "Introduction"). The
+// permutation groups the (token, slot) pairs by expert, tokens ascending
+// inside each expert, through a per-expert token bitmap: the result depends
+// only on ids, never on the order in which threads run.
+#include <cuda_runtime.h>
+#include <math.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// top-k of one token's logits by one warp
+// ---------------------------------------------------------------------------
+// Selection on logits is the same as selection on softmax probabilities
+// (exp is increasing); ties go to the lower expert id. The kept weights are
+// p_j / sum(p_sel) = exp(l_j - l_max) / sum exp(l_sel - l_max) in fp32.
+__device__ void topk_warp(const float *logits_row, int E, int k, int32_t *ids_out, float *w_out, bool bypass_l1) {
+    const int lane = threadIdx.x & 31;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int e = lane + 32 * i;
+        v[i] = (e < E) ? (bypass_l1 ? __ldcg(logits_row + e) : logits_row[e]) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float lmax = 0.f, sum = 0.f;
+    float my_val = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int e = lane + 32 * i;
+            bool ok = (e < E) && !((taken >> i) & 1u);
+            if (ok && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (j == 0) lmax = bv;
+        float ex = expf(bv - lmax);
+        sum += ex;
+        if (lane == j) {
+            my_val = ex;
+            my_id = bi;
+        }
+    }
+    if (lane < k) {
+        ids_out[lane] = my_id;
+        w_out[lane] = my_val / sum;
+    }
+}
+
+// ---------------------------------------------------------------------------
+// permutation by one CTA
+// ---------------------------------------------------------------------------
+// Shared memory needed: (4 * (E + 1) * 4) + E * words * 4 bytes, words = chunk / 32.
+struct PermSmem {
+    int32_t *cnt, *off, *run, *scratch;
+    uint32_t *bm;
+    int words;  // bitmap words per expert (chunk of tokens = 32 * words)
+};
+
+// Exclusive scan of a[0..n) (n <= 256) by warp 0; returns the total. Only
+// lanes of warp 0 call it.
+__device__ int warp0_exclusive_scan(const int32_t *a, int32_t *out, int n, int lane) {
+    int vals[8];
+    int local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int idx = lane * 8 + i;
+        vals[i] = idx < n ? a[idx] : 0;
+        local += vals[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        int idx = lane * 8 + i;
+        if (idx < n) out[idx] = run;
+        run += vals[i];
+    }
+    return __shfl_sync(0xFFFFFFFFu, incl, 31);
+}
+
+__device__ void permute_block(const int32_t *ids, int T, int k, int E, const Workspace &ws, PermSmem sm) {
+    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
+    for (int e = tid; e < E; e += nth) sm.cnt[e] = 0;
+    __syncthreads();
+    const int Tk = T * k;
+    for (int i = tid; i < Tk; i += nth) {
+        int e = ids[i];
+        if ((unsigned)e < (unsigned)E)
+            atomicAdd(&sm.cnt[e], 1);
+        else
+            atomicOr(&ws.ctrl->err, ERRBIT_RANGE);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int total = warp0_exclusive_scan(sm.cnt, sm.off, E, lane);
+        if (lane == 0) sm.off[E] = total;
+        // experts with tokens, ascending
+        for (int e = lane; e < E; e += 32) sm.scratch[e] = sm.cnt[e] > 0 ? 1 : 0;
+        __syncwarp();
+        int nu = warp0_exclusive_scan(sm.scratch, sm.run, E, lane);
+        __syncwarp();
+        for (int e = lane; e < E; e += 32)
+            if (sm.cnt[e] > 0) ws.uniq[sm.run[e]] = e;
+        // 128-row tiles per expert (prefill grouped GEMM)
+        for (int e = lane; e < E; e += 32) sm.scratch[e] = (sm.cnt[e] + 127) >> 7;
+        __syncwarp();
+        int nt = warp0_exclusive_scan(sm.scratch, ws.tile_off, E, lane);
+        if (lane == 0) {
+            ws.tile_off[E] = nt;
+            ws.ctrl->n_uniq = nu;
+            ws.ctrl->n_tiles_gu = nt;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += nth) {
+        ws.counts[e] = sm.cnt[e];
+        ws.offsets[e] = sm.off[e];
+        sm.run[e] = 0;
+    }
+    if (tid == 0) ws.offsets[E] = sm.off[E];
+    const int chunk = sm.words * 32;
+    for (int base = 0; base < T; base += chunk) {
+        const int nt = min(chunk, T - base);
+        for (int i = tid; i < E * sm.words; i += nth) sm.bm[i] = 0u;
+        __syncthreads();
+        for (int i = tid; i < nt * k; i += nth) {
+            int t = base + i / k;
+            int e = ids[(size_t)t * k + (i % k)];
+            if ((unsigned)e < (unsigned)E) {
+                int tl = t - base;
+                atomicOr(&sm.bm[e * sm.words + (tl >> 5)], 1u << (tl & 31));
+            }
+        }
+        __syncthreads();
+        for (int e = warp; e < E; e += nwarps) {
+            int run = sm.run[e];
+            const int row0 = sm.off[e];
+            for (int wb = 0; wb < sm.words; wb += 32) {
+                int wi = wb + lane;
+                uint32_t word = wi < sm.words ? sm.bm[e * sm.words + wi] : 0u;
+                int c = __popc(word);
+                int incl = c;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                int r = run + incl - c;
+                while (word) {
+                    int b = __ffs(word) - 1;
+                    word &= word - 1;
+                    int t = base + wi * 32 + b;
+                    int row = row0 + r;
+                    ws.perm[row] = t;
+                    for (int j = 0; j < k; ++j)
+                        if (ids[(size_t)t * k + j] == e) ws.pos[(size_t)t * k + j] = row;
+                    ++r;
+                }
+                run += __shfl_sync(0xFFFFFFFFu, incl, 31);
+            }
+            if (lane == 0) sm.run[e] = run;
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Small-T route: router GEMV on all CTAs; the last CTA to finish runs top-k
+// and the permutation (one launch for the whole routing step).
+// ---------------------------------------------------------------------------
+constexpr int kRouteSmallThreads = 256;
+constexpr int kRouteExpertsPerCta = 2;
+
+template <int TM>
+__global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(const uint16_t *__restrict__ x,
+                                                                         const uint16_t *__restrict__ wr,
+                                                                         const float *__restrict__ bias, int T, int d,
+                                                                         int E, int k, Workspace ws) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ float part[kRouteExpertsPerCta][4][TM];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int eps = warp >> 2, q = warp & 3;
+    const int e = blockIdx.x * kRouteExpertsPerCta + eps;
+    const int nvec_q = d / 32;  // 16-byte vectors per quarter row
+    float acc[TM];
+#pragma unroll
+    for (int t = 0; t < TM; ++t) acc[t] = 0.f;
+    if (e < E) {
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)e * d) + q * nvec_q;
+        for (int v = lane; v < nvec_q; v += 32) {
+            uint4 wv = __ldg(wrow + v);
+            float wf[8] = {bf16lo(wv.x), bf16hi(wv.x), bf16lo(wv.y), bf16hi(wv.y),
+                           bf16lo(wv.z), bf16hi(wv.z), bf16lo(wv.w), bf16hi(wv.w)};
+#pragma unroll
+            for (int t = 0; t < TM; ++t) {
+                if (t < T) {
+                    uint4 xv = __ldg(reinterpret_cast<const uint4 *>(x + (size_t)t * d) + q * nvec_q + v);
+                    acc[t] = fmaf(wf[0], bf16lo(xv.x), acc[t]);
+                    acc[t] = fmaf(wf[1], bf16hi(xv.x), acc[t]);
+                    acc[t] = fmaf(wf[2], bf16lo(xv.y), acc[t]);
+                    acc[t] = fmaf(wf[3], bf16hi(xv.y), acc[t]);
+                    acc[t] = fmaf(wf[4], bf16lo(xv.z), acc[t]);
+                    acc[t] = fmaf(wf[5], bf16hi(xv.z), acc[t]);
+                    acc[t] = fmaf(wf[6], bf16lo(xv.w), acc[t]);
+                    acc[t] = fmaf(wf[7], bf16hi(xv.w), acc[t]);
+                }
+            }
+        }
+    }
+#pragma unroll
+    for (int t = 0; t < TM; ++t) {
+        float s = warp_sum(acc[t]);
+        if (lane == 0) part[eps][q][t] = s;
+    }
+    __syncthreads();
+    if (tid < kRouteExpertsPerCta * TM) {
+        int ee = tid / TM, t = tid % TM;
+        int eg = blockIdx.x * kRouteExpertsPerCta + ee;
+        if (eg < E && t < T) {
+            float l = ((part[ee][0][t] + part[ee][1][t]) + part[ee][2][t]) + part[ee][3][t];
+            if (bias) l += bias[eg];
+            ws.logits[(size_t)t * E + eg] = l;
+        }
+    }
+    // last-CTA hand-off: every CTA publishes its logits, counts itself in;
+    // the CTA that completes the count runs the rest of the routing step.
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&ws.ctrl->route_done, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    if (tid == 0) ws.ctrl->route_done = 0u;
+    for (int t = warp; t < T; t += kRouteSmallThreads / 32)
+        topk_warp(ws.logits + (size_t)t * E, E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, true);
+    __syncthreads();
+    int32_t *si = reinterpret_cast<int32_t *>(smem_raw);
+    PermSmem sm{si, si + (E + 1), si + 2 * (E + 1), si + 3 * (E + 1),
+                reinterpret_cast<uint32_t *>(si + 4 * (E + 1)), 1};
+    permute_block(ws.ids, T, k, E, ws, sm);
+}
+
+static size_t perm_smem_bytes(int E, int words) { return (size_t)4 * (E + 1) * 4 + (size_t)E * words * 4; }
+
+cudaError_t launch_route_small(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st) {
+    int grid = (L.E + kRouteExpertsPerCta - 1) / kRouteExpertsPerCta;
+    size_t smem = perm_smem_bytes(L.E, 1);
+#define MOE_ROUTE_SMALL(TMV) \
+    route_small_kernel<TMV><<<grid, kRouteSmallThreads, smem, st>>>(x, L.wr, L.bias, T, L.d, L.E, L.k, ws)
+    if (T <= 1)
+        MOE_ROUTE_SMALL(1);
+    else if (T <= 2)
+        MOE_ROUTE_SMALL(2);
+    else if (T <= 4)
+        MOE_ROUTE_SMALL(4);
+    else if (T <= 8)
+        MOE_ROUTE_SMALL(8);
+    else if (T <= 16)
+        MOE_ROUTE_SMALL(16);
+    else if (T <= 32)
+        MOE_ROUTE_SMALL(32);
+    else
+        return cudaErrorInvalidValue;
+#undef MOE_ROUTE_SMALL
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Large-T route: router GEMM on the tensor cores (prefill.cu), a top-k kernel
+// (one warp per token) and a one-CTA permutation kernel.
+// ---------------------------------------------------------------------------
+__global__ void topk_kernel(const float *__restrict__ logits, int T, int E, int k, int32_t *ids, float *w) {
+    int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
+    if (t >= T) return;
+    topk_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k, false);
+}
+
+constexpr int kPermWords = 64;  // 2048 tokens per bitmap chunk
+
+__global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, Workspace ws) {
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    int32_t *si = reinterpret_cast<int32_t *>(smem_raw);
+    PermSmem sm{si, si + (E + 1), si + 2 * (E + 1), si + 3 * (E + 1),
+                reinterpret_cast<uint32_t *>(si + 4 * (E + 1)), kPermWords};
+    permute_block(ws.ids, T, k, E, ws, sm);
+}
+
+cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
+                               int *launches) {
+    cudaError_t e = launch_router_gemm(L, ws, x, T, st);
+    if (e != cudaSuccess) return e;
+    topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(ws.logits, T, L.E, L.k, ws.ids, ws.w);
+    size_t smem = perm_smem_bytes(L.E, kPermWords);
+    static bool attr_set = false;
+    if (!attr_set) {
+        cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        attr_set = true;
+    }
+    permute_kernel<<<1, 1024, smem, st>>>(T, L.k, L.E, ws);
+    *launches += 3;
+    return cudaGetLastError();
+}
+
+}  // namespace moe
