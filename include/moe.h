@@ -155,6 +155,31 @@ moe_status moe_profile_begin(moe_layer *layer, int max_forwards);
 moe_status moe_profile_end(moe_layer *layer, float *ms_host, int max_kernels, int *n_forwards,
                            int *n_kernels);
 
+/* The pages have no counterpart to this call; it serves callers that cannot
+ * allocate device memory (a plugin inside an inference server or engine that
+ * owns all device memory and hands it only input and output buffers, or a
+ * real-time loop that forbids allocation after start-up).
+ *
+ * Same result as moe_forward for 1 <= T <= 16 tokens, with no layer object
+ * and no workspace: the scratch lives in one static device array of
+ * MOE_STATIC_SCRATCH_BYTES that every GPU which loads libmoe.so holds until
+ * the process exits. The call allocates nothing (no cudaMalloc, no
+ * allocating library routine). desc is read on the host during the call only;
+ * its max_tokens is not used. x [T, d] and out [T, d] are bf16 device
+ * buffers of the caller.
+ * - The first call on a device, with that device current, looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.
+ * - Every call shares the one array and clears its control words at the start
+ *   (an async memset on `stream`): calls that overlap on the GPU race, so
+ *   issue them on one stream or otherwise order them.
+ * - Shapes whose scratch exceeds MOE_STATIC_SCRATCH_BYTES, or T > 16, return
+ *   MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG before any GPU work.
+ * - Device-side error bits are not reported (use moe_forward for that). */
+#define MOE_STATIC_SCRATCH_BYTES (8u << 20)
+moe_status moe_forward_static_scratch(const moe_layer_desc *desc, const void *x, void *out, int T,
+                                      void *stream);
+
 moe_status moe_layer_destroy(moe_layer *layer);
 
 const char *moe_status_string(moe_status s);

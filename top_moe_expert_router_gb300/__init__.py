@@ -79,6 +79,7 @@ def load(path: str | None = None):
             "moe_profile_begin": ([vp, i], st),
             "moe_profile_end": ([vp, vp, i, ctypes.POINTER(i), ctypes.POINTER(i)], st),
             "moe_layer_destroy": ([vp], st),
+            "moe_forward_static_scratch": ([ctypes.POINTER(MoeLayerDesc), vp, vp, i, vp], st),
             "moe_status_string": ([st], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():

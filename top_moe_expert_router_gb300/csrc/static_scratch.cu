@@ -1,0 +1,108 @@
+// static_scratch.cu — the decode forward for callers that cannot allocate
+// device memory.
+//
+// Some callers cannot call cudaMalloc: a plugin inside a host application
+// (an inference server or engine) that owns all device memory and hands the
+// plugin only its input and output buffers, or a real-time loop in which
+// allocating after start-up is forbidden. moe_forward_static_scratch() gives
+// them the small-batch layer forward (T <= 16) without a caller workspace:
+// its scratch (routing records, h, expert outputs, control words) lives in
+// the file-scope device array below, which every GPU that loads this library
+// holds until the process exits.
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "common.cuh"
+
+namespace {
+
+using namespace moe;
+
+// Scratch of the static-scratch forward, shared by every call on a device.
+static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxDevices = 64;
+void *g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch, per device
+int g_num_sms[kMaxDevices];
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+// One-time set-up per device, with that device current: the host-side name
+// g_static_scratch is only a stand-in, so the kernels get the device address.
+moe_status device_setup(int dev) {
+    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
+    if (g_scratch_ptr[dev]) return MOE_OK;
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
+    g_num_sms[dev] = sms;
+    g_scratch_ptr[dev] = ptr;
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, const void *x, void *out, int T,
+                                                 void *stream) {
+    size_t ignore = 0;
+    moe_status s = moe_workspace_size(desc, &ignore);  // shape checks only, no GPU work
+    if (s != MOE_OK) return s;
+    if (!x || !out || !aligned16(x) || !aligned16(out) || x == out || T < 1 || T > 16 || !desc->w_router ||
+        !aligned16(desc->w_router))
+        return MOE_ERR_INVALID_ARG;
+    if (desc->fmt == MOE_W_BF16) {
+        if (!desc->w_gate || !desc->w_up || !desc->w_down || !aligned16(desc->w_gate) || !aligned16(desc->w_up) ||
+            !aligned16(desc->w_down))
+            return MOE_ERR_INVALID_ARG;
+    } else {
+        const void *p[] = {desc->q_gate, desc->q_up, desc->q_down, desc->s_gate, desc->s_up,
+                           desc->s_down, desc->g_gate, desc->g_up,  desc->g_down};
+        for (const void *q : p)
+            if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+    }
+    // the tokens' rows sit in shared memory next to a ring of at least two stages
+    if ((size_t)T * desc->d * 2 + 2 * (4 * (size_t)desc->d * 2) + 4096 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
+    const Workspace need = workspace_layout(nullptr, desc->d, desc->E, desc->top_k, desc->I, T);
+    if (need.bytes > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+    s = device_setup(dev);
+    if (s != MOE_OK) return s;
+
+    LayerDev L{};
+    L.d = desc->d;
+    L.E = desc->E;
+    L.k = desc->top_k;
+    L.I = desc->I;
+    L.max_T = T;
+    L.fmt = desc->fmt;
+    L.wr = (const uint16_t *)desc->w_router;
+    L.bias = desc->router_bias;
+    L.wg = (const uint16_t *)desc->w_gate;
+    L.wu = (const uint16_t *)desc->w_up;
+    L.wd = (const uint16_t *)desc->w_down;
+    L.qg = desc->q_gate;
+    L.qu = desc->q_up;
+    L.qd = desc->q_down;
+    L.sg = desc->s_gate;
+    L.su = desc->s_up;
+    L.sd = desc->s_down;
+    L.gg = desc->g_gate;
+    L.gu = desc->g_up;
+    L.gd = desc->g_down;
+    L.num_sms = g_num_sms[dev];
+    const Workspace ws = workspace_layout(g_scratch_ptr[dev], L.d, L.E, L.k, L.I, T);
+
+    cudaStream_t st = (cudaStream_t)stream;
+    // the array keeps the previous call's contents: the control words (error
+    // bits, the router's arrival counter) must start at zero
+    if (cudaMemsetAsync(ws.ctrl, 0, sizeof(Control), st) != cudaSuccess) return MOE_ERR_CUDA;
+    const uint16_t *xs = (const uint16_t *)x;
+    cudaError_t e = launch_route_small(L, ws, xs, T, st);
+    if (e == cudaSuccess) e = launch_decode_gateup(L, ws, xs, T, st);
+    if (e == cudaSuccess) e = launch_decode_down(L, ws, xs, T, st);
+    if (e == cudaSuccess) e = launch_combine(L, ws, nullptr, (uint16_t *)out, T, st);
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
