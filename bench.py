@@ -256,7 +256,7 @@ def run_ours(args):
         import dataclasses
         w = dataclasses.replace(w, E=args.experts)
     if w.layers != 1 or w.fmt != "bf16":
-        raise SystemExit(f"bench.py: workload {w.name} is not a single bf16 layer")
+        return run_stack(args, w, moe, device, dist, rank, world, local_rank)
     gl, host = build_gpu_layer(moe, w, device)
     # each rank draws its own token pool (distinct rows of the token stream)
     pool_np = [datagen.tokens(w, w.T, start_row=(rank * POOL + i) * w.T) for i in range(POOL)]
@@ -310,7 +310,15 @@ def run_ours(args):
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
     step_gbs = float(layer_bytes.sum() / total_s / 1e9)
-    if prof.shape[1] == 4:
+    if prof.shape[1] == 1:
+        # the whole layer is one persistent kernel: router, routing, expert stream, combine
+        ly_ms = prof[:, 0].astype(np.float64)
+        ly_gbs = float(layer_bytes.mean() / (ly_ms.mean() / 1e3) / 1e9)
+        roofline = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": ly_gbs, "peak": hbm,
+                    "unit": "GB/s", "frac": ly_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                    "bytes_per_launch": float(layer_bytes.mean()), "ms_per_launch": float(ly_ms.mean())}
+        kernel_ms = {"layer": float(ly_ms.mean())}
+    elif prof.shape[1] == 4:
         gu_ms = prof[:, 1].astype(np.float64)
         gu_gbs = float(gateup_bytes.mean() / (gu_ms.mean() / 1e3) / 1e9)
         roofline = {"kernel": "decode_gateup_kernel", "bound": "hbm", "achieved": gu_gbs, "peak": hbm,
@@ -372,6 +380,126 @@ def run_ours(args):
                               "unique_experts_per_step": float(U.mean()), "kernel_ms": kernel_ms},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "gpu_launches": launches,
+            "clocks": clk,
+        }
+        print(json.dumps(line))
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def run_stack(args, w, moe, device, dist, rank, world, local_rank):
+    """Stacked NVFP4 decode: every step runs the token batch through all
+    layers, each RMSNorm -> MoE (NVFP4 experts) -> residual add."""
+    import torch
+
+    def bf(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+
+    layers, host_routers = [], []
+    for li in range(w.layers):
+        wr = datagen.router_weights(w, li)
+        g, u, d = datagen.expert_weights(w, li)
+        packs = {}
+        for name, arr in (("gate", g), ("up", u), ("down", d)):
+            dev = bf(arr)
+            q, s, gs = moe.quantize_nvfp4(dev)
+            packs["q_" + name], packs["s_" + name], packs["g_" + name] = q, s, gs
+            del dev
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        layers.append(moe.MoeLayer(bf(wr), nvfp4=packs, top_k=w.k, max_tokens=max(w.T, 16)))
+        host_routers.append(wr)
+    pool_np = [datagen.tokens(w, w.T, start_row=(rank * POOL + i) * w.T) for i in range(POOL)]
+    pool = [bf(p) for p in pool_np]
+    xcur = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
+    ubuf = torch.empty_like(xcur)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream()
+
+    def step(x0, route_log=None):
+        xcur.copy_(x0)
+        for gl in layers:
+            moe.rmsnorm(xcur, 1e-6, out=ubuf)
+            if route_log is not None:
+                route_log.append(int((gl.route(ubuf)["counts"] > 0).sum().item()))
+            gl.forward(ubuf, out=xcur, res=xcur)
+
+    for s in range(args.warmup):
+        flush.zero_()
+        step(pool[s % POOL])
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for gl in layers:
+        gl.profile_begin(args.steps)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    launches = 0
+    for s in range(args.steps):
+        flush.zero_()
+        evs[s][0].record(stream)
+        step(pool[s % POOL])
+        evs[s][1].record(stream)
+        launches += w.layers * (1 + layers[0].last_launch_count())
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = np.array([a.elapsed_time(b) for a, b in evs])
+    profs = [gl.profile_end() for gl in layers]             # each [steps, 4]
+    for gl in layers:
+        assert gl.device_status() == 0
+    total_s = float(step_ms.sum()) / 1e3
+    value, t_max = aggregate(w.T * args.steps, total_s, dist, device)
+    # unique experts per layer per step, from an untimed replay of the pool
+    U = np.zeros((POOL, w.layers))
+    for i in range(POOL):
+        log = []
+        step(pool[i], route_log=log)
+        U[i] = log
+    torch.cuda.synchronize()
+    Us = np.array([U[s % POOL] for s in range(args.steps)])      # [steps, layers]
+    eb = w.expert_bytes_nvfp4
+    peaks, peak_src = load_peaks()
+    hbm = peaks["hbm_gbs"]
+    layer_bytes = Us * eb + w.E * w.d * 2                           # [steps, layers]
+    if profs[0].shape[1] == 1:
+        kname = "decode_layer_kernel (NVFP4)"
+        k_bytes = layer_bytes
+        k_ms = np.stack([p[:, 0] for p in profs], axis=1).astype(np.float64)
+        kms = {"layer": float(k_ms.mean())}
+    else:
+        kname = "decode_gateup_kernel (NVFP4)"
+        k_bytes = Us * 2 * w.I * (w.d // 2 + w.d // 16)             # gate + up codes and scales
+        k_ms = np.stack([p[:, 1] for p in profs], axis=1).astype(np.float64)
+        kms = {name: float(np.mean([p[:, i].mean() for p in profs]))
+               for i, name in enumerate(["route", "gateup", "down", "combine"])}
+    gu_bytes, gu_ms = k_bytes, k_ms
+    gu_gbs = float(gu_bytes.sum() / (gu_ms.sum() / 1e3) / 1e9)
+    step_bytes = layer_bytes.sum(1)
+    step_gbs = float(step_bytes.sum() / total_s / 1e9)
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 experts, bf16 activations, fp32 accumulate",
+            "data": "synthetic",
+            "config": workload_config(w, parallelism=f"replicas x{world}",
+                                      l2="flushed before every step (256 MiB write), outside the step events",
+                                      step="8 x (RMSNorm, MoE, residual)"),
+            "roofline": {"kernel": kname, "bound": "hbm", "achieved": gu_gbs, "peak": hbm,
+                         "unit": "GB/s", "frac": gu_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                         "bytes_per_launch": float(gu_bytes.mean()), "ms_per_launch": float(gu_ms.mean())},
+            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
+                              "frac": step_gbs / hbm, "bytes_per_step": float(step_bytes.mean()),
+                              "unique_experts_per_layer": float(Us.mean()), "kernel_ms_per_layer": kms},
+            "cpu_baseline": None,
+            "e2e": None,
             "gpu_launches": launches,
             "clocks": clk,
         }

@@ -84,6 +84,11 @@ typedef struct {
     const uint8_t *s_gate, *s_up; /* [E, I, d/16] */
     const uint8_t *s_down;        /* [E, d, I/16] */
     const float *g_gate, *g_up, *g_down; /* [E] per-tensor fp32 scales */
+    /* 0: the plain weighted sum. 1: each expert's output is RMS-normalised
+     * (Y / sqrt(mean(Y^2) + 1e-6), no learned scale) before the weighted sum,
+     * a reading of "Muse Spark normalises each expert's output, then combines"
+     * ("TensorSharp Muse Spark benchmark", section "Performance"). */
+    int expert_out_norm;
 } moe_layer_desc;
 
 /* Bytes of device workspace the layer needs (for max_tokens). No GPU work. */

@@ -47,6 +47,7 @@ class OrcLayer(ctypes.Structure):
         ("q_gate", ctypes.c_void_p), ("q_up", ctypes.c_void_p), ("q_down", ctypes.c_void_p),
         ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
         ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p),
+        ("expert_norm", ctypes.c_int),
     ]
 
 
@@ -194,7 +195,8 @@ class Layer:
     s_gate/s_up [E, I, d/16], s_down [E, d, I/16] (uint8) and g_gate/g_up/g_down [E] fp32.
     """
 
-    def __init__(self, w_router, gate=None, up=None, down=None, router_bias=None, k=8, nvfp4=None):
+    def __init__(self, w_router, gate=None, up=None, down=None, router_bias=None, k=8, nvfp4=None,
+                 expert_norm=False):
         self.w_router = _c(w_router, np.uint16)
         self.router_bias = _c(router_bias, np.float32)
         self.E, self.d = self.w_router.shape
@@ -217,6 +219,7 @@ class Layer:
             for key, v in f.items():
                 setattr(s, key, _p(v))
         s.I = self.I
+        s.expert_norm = 1 if expert_norm else 0
         self._s = s
 
     def forward(self, x, tokens=None, forced_ids=None, want_Y=False):

@@ -53,7 +53,13 @@ typedef struct {
     const uint8_t *s_gate, *s_up;     /* [E, I, d/16] E4M3 block scales */
     const uint8_t *s_down;            /* [E, d, I/16] */
     const float *g_gate, *g_up, *g_down; /* [E] per-tensor fp32 scales */
+    int expert_norm;                  /* 1: RMS-normalise each expert output before the sum */
 } orc_layer;
+
+/* RMS normalisation of an expert output before the weighted sum, eps 1e-6,
+ * no learned scale. Reading of "Muse Spark normalises each expert's output,
+ * then combines" ("TensorSharp Muse Spark benchmark", section "Performance"). */
+#define ORC_EXPERT_NORM_EPS 1e-6
 
 /* ------------------------------------------------------------------------- */
 /* number formats                                                             */
@@ -435,14 +441,26 @@ void orc_forward(const orc_layer *L, const uint16_t *x, int T,
         orc_expert_ffn(L, ids_out[item], xs + (long long)a * d, h, Yall + item * d);
         free(h);
     }
+    /* per-slot factor: 1, or 1 / sqrt(mean(Y^2) + eps) when normalising */
+    double *fac = (double *)malloc(sizeof(double) * (size_t)n * k);
+    for (long long item = 0; item < (long long)n * k; ++item) {
+        fac[item] = 1.0;
+        if (L->expert_norm) {
+            double ss = 0.0;
+            for (int c = 0; c < d; ++c)
+                ss += Yall[item * d + c] * Yall[item * d + c];
+            fac[item] = 1.0 / sqrt(ss / d + ORC_EXPERT_NORM_EPS);
+        }
+    }
     for (int a = 0; a < n; ++a) {
         for (int c = 0; c < d; ++c) {
             double acc = 0.0;
             for (int j = 0; j < k; ++j)
-                acc += w_out[(long long)a * k + j] * Yall[((long long)a * k + j) * d + c];
+                acc += w_out[(long long)a * k + j] * (Yall[((long long)a * k + j) * d + c] * fac[(long long)a * k + j]);
             y_out[(long long)a * d + c] = acc;
         }
     }
+    free(fac);
     if (!Y_out)
         free(Yall);
     free(lg);

@@ -115,7 +115,7 @@ def test_deterministic_and_launch_count(tiny):
     host, gl = tiny
     xd = to_dev_bf16(datagen.tokens(host.w, 5, start_row=900))
     a = gl.forward(xd).clone()
-    assert gl.last_launch_count() == 4        # route, gate/up, down, combine
+    assert gl.last_launch_count() == 1        # the whole small-batch layer is one persistent kernel
     b = gl.forward(xd)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))

@@ -400,3 +400,38 @@ def test_residual_add():
     x = datagen.f32_to_bf16(np.array([1.0, -2.0, 0.5], np.float32))
     out = oracle.residual_add(x, np.array([0.25, 0.5, -0.5]))
     assert datagen.bf16_to_f32(out).tolist() == [1.25, -1.5, 0.0]
+
+
+# --------------------------------------------------------------------------
+# per-expert output normalisation before the combine (optional variant)
+# --------------------------------------------------------------------------
+
+def test_expert_norm_identical_experts_closed_form():
+    wr = datagen.router_weights(TINY)
+    g1, u1, d1 = (a[:1] for a in datagen.expert_weights(TINY, experts=[0]))
+    rep = lambda a: np.repeat(a, TINY.E, 0)
+    L = oracle.Layer(wr, rep(g1), rep(u1), rep(d1), k=8, expert_norm=True)
+    x = datagen.tokens(TINY, 4)
+    r = L.forward(x)
+    for t in range(4):
+        f = _torch_ffn(x[t], g1[0], u1[0], d1[0])
+        ref = f / np.sqrt(np.mean(f * f) + 1e-6)
+        np.testing.assert_allclose(r["y"][t], ref, rtol=1e-10, atol=1e-14)
+
+
+def test_expert_norm_is_scale_invariant_and_bounded():
+    L, (wr, g, u, d) = _tiny_layer()
+    Ln = oracle.Layer(wr, g, u, d, k=8, expert_norm=True)
+    # W_down scaled by 2^8 and 2^9 (exact in bf16): mean(Y^2) then dwarfs eps
+    big = [oracle.Layer(wr, g, u, datagen.f32_to_bf16(datagen.bf16_to_f32(d) * s), k=8, expert_norm=True)
+           for s in (256.0, 512.0)]
+    x = datagen.tokens(TINY, 8)
+    a = Ln.forward(x, want_Y=True)
+    b1, b2 = (L_.forward(x)["y"] for L_ in big)
+    # RMS normalisation removes the scale of W_down
+    np.testing.assert_allclose(b2, b1, rtol=1e-6, atol=1e-7)
+    assert np.abs(b1 - 2 * b1).max() > 1e-3
+    # each slot contributes unit RMS: the combined RMS is at most sum(w) = 1
+    assert (np.sqrt((a["y"] ** 2).mean(1)) <= 1.0 + 1e-9).all()
+    # the raw expert outputs are the same as without the normalisation
+    np.testing.assert_allclose(a["Y"], L.forward(x, want_Y=True)["Y"], rtol=0, atol=0)

@@ -40,6 +40,7 @@ class MoeLayerDesc(ctypes.Structure):
         ("q_gate", ctypes.c_void_p), ("q_up", ctypes.c_void_p), ("q_down", ctypes.c_void_p),
         ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
         ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p),
+        ("expert_out_norm", ctypes.c_int),
     ]
 
 
@@ -125,12 +126,13 @@ class MoeLayer:
     """
 
     def __init__(self, w_router, *, w_gate=None, w_up=None, w_down=None, nvfp4=None,
-                 router_bias=None, top_k=8, max_tokens=16):
+                 router_bias=None, top_k=8, max_tokens=16, expert_out_norm=False):
         lib = load()
         E, d = w_router.shape
         self.d, self.E, self.k, self.max_tokens = d, E, top_k, max_tokens
         desc = MoeLayerDesc()
         desc.d, desc.E, desc.top_k, desc.max_tokens = d, E, top_k, max_tokens
+        desc.expert_out_norm = 1 if expert_out_norm else 0
         self._keep = [w_router, router_bias]
         desc.w_router = _ptr(w_router)
         desc.router_bias = _ptr(router_bias)

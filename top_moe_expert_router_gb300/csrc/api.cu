@@ -107,6 +107,18 @@ moe_status forward_impl(moe_layer *ly, const uint16_t *x, const uint16_t *res, u
     int launches = 0;
     const int tdec = decode_max_tokens(L.d);
     if (T > tdec && prefill_supported(L)) return forward_prefill(ly, x, res, out, T, st);
+    if (T <= tdec) {
+        // the whole layer in one persistent launch
+        prof_mark(ly, 0, st);
+        cudaError_t e = launch_decode_fused(L, ly->ws, x, res, out, T, st);
+        prof_mark(ly, 1, st);
+        ly->last_launches = L.expert_norm ? 2 : 1;
+        if (ly->prof_count < ly->prof_max) {
+            ly->prof_nk = 1;
+            ++ly->prof_count;
+        }
+        return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
     // Token chunks of at most tdec tokens run the streaming expert stage; a
     // chunk is a full layer forward (route, experts, combine) of its tokens.
     const bool single = T <= tdec;
@@ -186,6 +198,7 @@ moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t 
     L.gu = desc->g_up;
     L.gd = desc->g_down;
     L.num_sms = sms;
+    L.expert_norm = desc->expert_out_norm ? 1 : 0;
     ly->ws = ws;
     ly->last_launches = 0;
     *out = ly;

@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"
 
 namespace moe {
 
@@ -28,7 +28,10 @@ struct Control {
     int32_t n_uniq;          // number of experts with at least one token
     int32_t n_tiles_gu;      // prefill: gate/up tiles
     int32_t n_tiles_dn;      // prefill: down tiles
-    int32_t pad[59];
+    uint32_t grid_bar;       // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
+    uint32_t grid_exit;      // fused decode kernel: CTAs that finished
+    uint32_t pad[26];
+    uint32_t cb_rows[32];    // fused decode kernel: expert rows done per 256-column block of Y
 };
 
 struct Workspace {
@@ -47,6 +50,8 @@ struct Workspace {
     float *h;           // [max_T*k, I] fp32 (decode) / bf16 (prefill)
     float *Y;           // [max_T*k, d] fp32 expert outputs
     uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill)
+    int32_t *chunk_base;  // [ceil(max_T/256), E] per-chunk counts, then each chunk's first row per expert
+    uint32_t *chunk_bm;   // [ceil(max_T/256), E, 8] token bitmaps of each 256-token chunk
     size_t bytes;
 };
 
@@ -77,6 +82,9 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     ws.h = (float *)take(sizeof(float) * Tk * I);
     ws.Y = (float *)take(sizeof(float) * Tk * d);
     ws.xperm = (uint16_t *)take(sizeof(uint16_t) * Tk * d);
+    const size_t nchunks = ((size_t)max_T + 255) / 256;
+    ws.chunk_base = (int32_t *)take(sizeof(int32_t) * nchunks * E);
+    ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E * 8);
     ws.bytes = off;
     return ws;
 }
@@ -220,6 +228,7 @@ struct LayerDev {
     const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
     const float *gg, *gu, *gd;
     int num_sms;
+    int expert_norm;  // RMS-normalise each expert output before the weighted sum
 };
 
 // route.cu
@@ -229,6 +238,9 @@ cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const uin
 // decode.cu
 cudaError_t launch_decode_gateup(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
 cudaError_t launch_decode_down(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+// decode_fused.cu
+cudaError_t launch_decode_fused(const LayerDev &L, const Workspace &ws, const uint16_t *x, const uint16_t *res,
+                                uint16_t *out, int T, cudaStream_t st);
 // misc.cu
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
                            cudaStream_t st);

@@ -16,7 +16,12 @@
 // where r runs over the rows of the permuted (token, slot) order of expert e.
 // The flattened rows of all active experts are split evenly over the CTAs,
 // so every SM streams the same number of bytes whatever the routing.
-// Warp roles: warps 0..7 consume stages, warp 8 (one lane) produces them.
+// Warp roles: warp 8 (one lane) fills the ring; stage s is consumed by warp
+// s % ncons alone (a whole gate/up row pair, or four down rows; ncons <= 8),
+// so the consumer warps drain different stages at once and never wait for
+// each other. Both kernels are launched as programmatic dependents of the kernel
+// before them: their prologue overlaps its tail, and the down kernel starts
+// streaming its weights before the gate/up results it consumes are complete.
 //
 // Formats: bf16 rows, or NVFP4 rows (packed E2M1 codes + one E4M3 scale per 16
 // elements + one fp32 scale per tensor) dequantised in registers as they are
@@ -31,9 +36,8 @@ namespace moe {
 
 constexpr int kConsumerWarps = 8;
 constexpr int kDecodeThreads = 32 * (kConsumerWarps + 1);
-constexpr int kGuRowsPerStage = 2;   // gate/up: rows i per stage (each with gate and up)
-constexpr int kDnRowsPerStage = 8;   // down: rows c per stage
-constexpr int kMaxStages = 8;
+constexpr int kDnRows = 4;           // down: rows c per stage
+constexpr int kMaxStages = 16;
 constexpr int kSmemBudget = 227 * 1024;
 
 template <bool FP4>
@@ -48,25 +52,17 @@ struct DecodeArgs {
     const float *gg, *gu, *gd;
     int T, d, I, k;
     int nstages;
+    // Consumer warps in use; nstages is a multiple of ncons, so slot j is only
+    // ever consumed by warp j % ncons and each warp takes the phases of its own
+    // slots in order. A wait by phase parity is then never more than one phase
+    // ahead of the slot (bulk copies may complete out of issue order, so a
+    // slot shared between warps could show a stale phase of the same parity).
+    int ncons;
     Workspace ws;
 };
 
-// Segment bookkeeping: a CTA walks a contiguous range of flattened rows
-// g = u * R + row over the active experts u (R rows per expert); a stage never
-// crosses an expert boundary.
-struct StageCursor {
-    long long g, end;
-    int R, max_rows;
-    __device__ int next_len() const {
-        long long left_in_expert = R - (g % R);
-        long long left = end - g;
-        long long n = left < left_in_expert ? left : left_in_expert;
-        return (int)(n < max_rows ? n : max_rows);
-    }
-};
-
 // ---------------------------------------------------------------------------
-// dot helpers
+// helpers
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void unpack8(uint4 v, float f[8]) {
     f[0] = bf16lo(v.x); f[1] = bf16hi(v.x); f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
@@ -85,7 +81,19 @@ __device__ __forceinline__ float dot8(const float w[8], uint4 xv) {
     return a;
 }
 
-// 8 packed bytes -> 16 E2M1 values (exact in fp32)
+__device__ __forceinline__ float dot8h(const float w[8], float4 h0, float4 h1) {
+    float t = w[0] * h0.x;
+    t = fmaf(w[1], h0.y, t);
+    t = fmaf(w[2], h0.z, t);
+    t = fmaf(w[3], h0.w, t);
+    t = fmaf(w[4], h1.x, t);
+    t = fmaf(w[5], h1.y, t);
+    t = fmaf(w[6], h1.z, t);
+    t = fmaf(w[7], h1.w, t);
+    return t;
+}
+
+// 8 packed bytes -> 16 E2M1 values (exact in fp32), low nibble first
 __device__ __forceinline__ void unpack_fp4x16(uint2 q, float f[16]) {
     uint32_t words[2] = {q.x, q.y};
 #pragma unroll
@@ -95,7 +103,7 @@ __device__ __forceinline__ void unpack_fp4x16(uint2 q, float f[16]) {
             __nv_fp4x2_storage_t byte = (__nv_fp4x2_storage_t)((words[wi] >> (8 * b)) & 0xFFu);
             __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2(byte, __NV_E2M1);
             float2 p = __half22float2(*reinterpret_cast<__half2 *>(&hr));
-            f[wi * 8 + 2 * b] = p.x;      // low nibble: lower index
+            f[wi * 8 + 2 * b] = p.x;
             f[wi * 8 + 2 * b + 1] = p.y;
         }
     }
@@ -106,8 +114,32 @@ __device__ __forceinline__ float e4m3_to_f32(uint8_t s) {
     return __half2float(*reinterpret_cast<__half *>(&hr));
 }
 
+// Programmatic dependent launch: wait for the grid this one depends on (a
+// no-op when launched without the attribute); let the next grid launch.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Per-warp cache of the expert a stage belongs to.
+template <int TM>
+struct ExpertSeg {
+    int u = -1, e = 0, n_e = 0, row_base = 0;
+    int tok[TM];
+    __device__ __forceinline__ void load(const Workspace &ws, int uu, uint32_t *err) {
+        u = uu;
+        e = ws.uniq[uu];
+        n_e = ws.counts[e];
+        row_base = ws.offsets[e];
+        if (n_e > TM) {  // cannot happen when T <= TM
+            atomicOr(err, ERRBIT_RANGE);
+            n_e = TM;
+        }
+#pragma unroll
+        for (int r = 0; r < TM; ++r) tok[r] = (r < n_e) ? ws.perm[row_base + r] : 0;
+    }
+};
+
 // ---------------------------------------------------------------------------
-// gate/up kernel
+// gate/up kernel: stage s = row pair g_begin + s (gate row i and up row i)
 // ---------------------------------------------------------------------------
 template <int TM, bool FP4>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_gateup_kernel(DecodeArgs a) {
@@ -120,67 +152,56 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_gateup_kernel(Decode
     uint64_t *empty = full + kMaxStages;
     uint64_t *xbar = empty + kMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(xbar + 1);
-    float *red = reinterpret_cast<float *>(smem + 256);  // [2][RP][4][TM][2]
-    constexpr int kParts = kConsumerWarps / kGuRowsPerStage;
-    const size_t red_bytes = sizeof(float) * 2 * kGuRowsPerStage * kParts * TM * 2;
-    unsigned char *xs = smem + 256 + ((red_bytes + 127) / 128) * 128;
-    const size_t x_bytes = (size_t)a.T * d * 2;
+    unsigned char *xs = smem + 512;
+    const uint32_t x_bytes = (uint32_t)a.T * d * 2;
     unsigned char *ring = xs + ((x_bytes + 127) / 128) * 128;
-    const size_t rb = row_bytes<FP4>(d);
-    const size_t stage_bytes = 2 * kGuRowsPerStage * rb;
+    const uint32_t rb = (uint32_t)row_bytes<FP4>(d);
+    const uint32_t stage_bytes = 2 * rb;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], 1);
         }
         mbar_init(xbar, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dep_wait();      // routing results of the previous kernel
+    grid_dep_launch();
 
-    const long long G = (long long)a.ws.ctrl->n_uniq * I;
-    const long long g_begin = (long long)blockIdx.x * G / gridDim.x;
-    const long long g_end = (long long)(blockIdx.x + 1) * G / gridDim.x;
+    const int G = a.ws.ctrl->n_uniq * I;
+    const int g_begin = (int)((long long)blockIdx.x * G / gridDim.x);
+    const int n_st = (int)((long long)(blockIdx.x + 1) * G / gridDim.x) - g_begin;
 
     if (warp == kConsumerWarps) {
         // ------------------------------ producer ------------------------------
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            mbar_arrive_expect_tx(xbar, (uint32_t)x_bytes);
-            bulk_g2s(xs, a.x, (uint32_t)x_bytes, xbar, policy_evict_last());
-            StageCursor cur{g_begin, g_end, I, kGuRowsPerStage};
+            mbar_arrive_expect_tx(xbar, x_bytes);
+            bulk_g2s(xs, a.x, x_bytes, xbar, policy_evict_last());
             int s = 0;
-            bool ok = true;
-            while (cur.g < cur.end && ok) {
+            for (; s < n_st; ++s) {
                 const int slot = s % NS;
-                if (s >= NS) ok = mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag);
-                if (!ok) break;
-                const int n = cur.next_len();
-                const int u = (int)(cur.g / I), i0 = (int)(cur.g % I);
-                const int e = a.ws.uniq[u];
+                if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
+                const int g = g_begin + s;
+                const int u = g / I, i = g - u * I;
+                const size_t row = (size_t)a.ws.uniq[u] * I + i;
                 unsigned char *dst = ring + (size_t)slot * stage_bytes;
-                const size_t row0 = (size_t)e * I + i0;
+                mbar_arrive_expect_tx(&full[slot], stage_bytes);
                 if (!FP4) {
-                    const uint32_t nb = (uint32_t)(n * rb);
-                    mbar_arrive_expect_tx(&full[slot], 2 * nb);
-                    bulk_g2s(dst, a.wg + row0 * d, nb, &full[slot], pol);
-                    bulk_g2s(dst + kGuRowsPerStage * rb, a.wu + row0 * d, nb, &full[slot], pol);
+                    bulk_g2s(dst, a.wg + row * d, rb, &full[slot], pol);
+                    bulk_g2s(dst + rb, a.wu + row * d, rb, &full[slot], pol);
                 } else {
-                    const uint32_t nq = (uint32_t)(n * (d / 2)), ns_ = (uint32_t)(n * (d / 16));
-                    mbar_arrive_expect_tx(&full[slot], 2 * (nq + ns_));
-                    unsigned char *gq = dst, *gs = dst + kGuRowsPerStage * (d / 2);
-                    unsigned char *uq = dst + kGuRowsPerStage * rb, *us = uq + kGuRowsPerStage * (d / 2);
-                    bulk_g2s(gq, a.qg + row0 * (d / 2), nq, &full[slot], pol);
-                    bulk_g2s(gs, a.sg + row0 * (d / 16), ns_, &full[slot], pol);
-                    bulk_g2s(uq, a.qu + row0 * (d / 2), nq, &full[slot], pol);
-                    bulk_g2s(us, a.su + row0 * (d / 16), ns_, &full[slot], pol);
+                    const uint32_t nq = d / 2, nsb = d / 16;
+                    bulk_g2s(dst, a.qg + row * nq, nq, &full[slot], pol);
+                    bulk_g2s(dst + nq, a.sg + row * nsb, nsb, &full[slot], pol);
+                    bulk_g2s(dst + rb, a.qu + row * nq, nq, &full[slot], pol);
+                    bulk_g2s(dst + rb + nq, a.su + row * nsb, nsb, &full[slot], pol);
                 }
-                cur.g += n;
-                ++s;
             }
-            // drain: every copy issued must land before the CTA exits
+            // every copy issued must land before the CTA exits
             for (int j = (s > NS ? s - NS : 0); j < s; ++j) mbar_wait(&full[j % NS], (j / NS) & 1, err);
             mbar_wait(xbar, 0, err);
         }
@@ -188,118 +209,71 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_gateup_kernel(Decode
     }
 
     // -------------------------------- consumers --------------------------------
-    const int rr = warp / kParts, part = warp % kParts;
-    mbar_wait_or_abort(xbar, 0, err, abort_flag);
-    named_bar(1, 32 * kConsumerWarps);
-    if (*abort_flag) return;
-    StageCursor cur{g_begin, g_end, I, kGuRowsPerStage};
-    int s = 0;
-    int seg_u = -1, n_e = 0, row_base = 0, e = 0;
-    int tok[TM];
-#pragma unroll
-    for (int r = 0; r < TM; ++r) tok[r] = 0;
-    const int kpart = d / kParts;  // columns per part
-    while (cur.g < cur.end) {
+    if (warp >= a.ncons) return;
+    if (!mbar_wait_or_abort(xbar, 0, err, abort_flag)) return;
+    ExpertSeg<TM> seg;
+    for (int s = warp; s < n_st; s += a.ncons) {
         const int slot = s % NS;
-        const int n = cur.next_len();
-        const int u = (int)(cur.g / I), i0 = (int)(cur.g % I);
-        if (u != seg_u) {
-            seg_u = u;
-            e = a.ws.uniq[u];
-            n_e = a.ws.counts[e];
-            row_base = a.ws.offsets[e];
-            if (n_e > TM) {  // cannot happen when T <= TM
-                atomicOr(err, ERRBIT_RANGE);
-                n_e = TM;
-            }
-#pragma unroll
-            for (int r = 0; r < TM; ++r) tok[r] = (r < n_e) ? a.ws.perm[row_base + r] : 0;
-        }
-        const bool ok = mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag);
+        const int g = g_begin + s;
+        const int u = g / I, i = g - u * I;
+        if (u != seg.u) seg.load(a.ws, u, err);
+        if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) return;
         const unsigned char *st = ring + (size_t)slot * stage_bytes;
         float accg[TM], accu[TM];
 #pragma unroll
         for (int r = 0; r < TM; ++r) accg[r] = accu[r] = 0.f;
-        if (ok && rr < n) {
-            if (!FP4) {
-                const uint4 *gw = reinterpret_cast<const uint4 *>(st + rr * rb) + part * (kpart / 8);
-                const uint4 *uw = reinterpret_cast<const uint4 *>(st + (kGuRowsPerStage + rr) * rb) + part * (kpart / 8);
-                for (int v = lane; v < kpart / 8; v += 32) {
-                    float gf[8], uf[8];
-                    unpack8(gw[v], gf);
-                    unpack8(uw[v], uf);
+        if (!FP4) {
+            const uint4 *gw = reinterpret_cast<const uint4 *>(st);
+            const uint4 *uw = reinterpret_cast<const uint4 *>(st + rb);
+            for (int v = lane; v < d / 8; v += 32) {
+                float gf[8], uf[8];
+                unpack8(gw[v], gf);
+                unpack8(uw[v], uf);
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < n_e) {
-                            uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)tok[r] * d * 2)[part * (kpart / 8) + v];
-                            accg[r] += dot8(gf, xv);
-                            accu[r] += dot8(uf, xv);
-                        }
-                    }
-                }
-            } else {
-                const unsigned char *gq = st, *gs = st + kGuRowsPerStage * (d / 2);
-                const unsigned char *uq = st + kGuRowsPerStage * rb, *us = uq + kGuRowsPerStage * (d / 2);
-                // one 16-element block per lane iteration
-                const int nblk = kpart / 16, blk0 = part * nblk;
-                for (int b = lane; b < nblk; b += 32) {
-                    const int blk = blk0 + b;
-                    float gf[16], uf[16];
-                    unpack_fp4x16(*reinterpret_cast<const uint2 *>(gq + (size_t)rr * (d / 2) + blk * 8), gf);
-                    unpack_fp4x16(*reinterpret_cast<const uint2 *>(uq + (size_t)rr * (d / 2) + blk * 8), uf);
-                    const float sgb = e4m3_to_f32(gs[(size_t)rr * (d / 16) + blk]);
-                    const float sub = e4m3_to_f32(us[(size_t)rr * (d / 16) + blk]);
-#pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < n_e) {
-                            const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)tok[r] * d * 2) + blk * 2;
-                            uint4 x0 = xp[0], x1 = xp[1];
-                            float pg = dot8(gf, x0) + dot8(gf + 8, x1);
-                            float pu = dot8(uf, x0) + dot8(uf + 8, x1);
-                            accg[r] = fmaf(pg, sgb, accg[r]);
-                            accu[r] = fmaf(pu, sub, accu[r]);
-                        }
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v];
+                        accg[r] += dot8(gf, xv);
+                        accu[r] += dot8(uf, xv);
                     }
                 }
             }
-        }
-        float *rd = red + (size_t)(s & 1) * kGuRowsPerStage * kParts * TM * 2;
+        } else {
+            const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rb, *us = st + rb + d / 2;
+            for (int b = lane; b < d / 16; b += 32) {
+                float gf[16], uf[16];
+                unpack_fp4x16(*reinterpret_cast<const uint2 *>(gq + b * 8), gf);
+                unpack_fp4x16(*reinterpret_cast<const uint2 *>(uq + b * 8), uf);
+                const float sgb = e4m3_to_f32(gs[b]), sub = e4m3_to_f32(us[b]);
 #pragma unroll
-        for (int r = 0; r < TM; ++r) {
-            if (r < n_e) {
-                float sg_ = warp_sum(accg[r]);
-                float su_ = warp_sum(accu[r]);
-                if (lane == 0) {
-                    rd[((rr * kParts + part) * TM + r) * 2 + 0] = sg_;
-                    rd[((rr * kParts + part) * TM + r) * 2 + 1] = su_;
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + b * 2;
+                        const uint4 x0 = xp[0], x1 = xp[1];
+                        accg[r] = fmaf(dot8(gf, x0) + dot8(gf + 8, x1), sgb, accg[r]);
+                        accu[r] = fmaf(dot8(uf, x0) + dot8(uf + 8, x1), sub, accu[r]);
+                    }
                 }
             }
         }
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(&empty[slot]);
-        named_bar(1, 32 * kConsumerWarps);
-        if (*abort_flag) return;
-        // rows rr < n, tokens r < n_e: h = silu(g) * u
-        if (part == 0 && rr < n && lane < n_e) {
-            float g = 0.f, uu = 0.f;
+        if (lane == 0) mbar_arrive(&empty[slot]);   // the stage's shared memory is free again
+        const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
+        float hv = 0.f;
 #pragma unroll
-            for (int p = 0; p < kParts; ++p) {
-                g += rd[((rr * kParts + p) * TM + lane) * 2 + 0];
-                uu += rd[((rr * kParts + p) * TM + lane) * 2 + 1];
+        for (int r = 0; r < TM; ++r) {
+            if (r < seg.n_e) {
+                const float sg_ = warp_sum(accg[r]) * gsc;
+                const float su_ = warp_sum(accu[r]) * usc;
+                if (lane == r) hv = silu(sg_) * su_;
             }
-            if (FP4) {
-                g *= a.gg[e];
-                uu *= a.gu[e];
-            }
-            a.ws.h[(size_t)(row_base + lane) * I + i0 + rr] = silu(g) * uu;
         }
-        cur.g += n;
-        ++s;
+        if (lane < seg.n_e) a.ws.h[(size_t)(seg.row_base + lane) * I + i] = hv;
     }
 }
 
 // ---------------------------------------------------------------------------
-// down kernel
+// down kernel: stage s = kDnRows consecutive rows c of one expert
 // ---------------------------------------------------------------------------
 template <int TM, bool FP4>
 __global__ void __launch_bounds__(kDecodeThreads, 1) decode_down_kernel(DecodeArgs a) {
@@ -311,169 +285,164 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_down_kernel(DecodeAr
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
     uint64_t *empty = full + kMaxStages;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(empty + kMaxStages);
-    float *hs = reinterpret_cast<float *>(smem + 256);  // [TM][I]
-    const size_t h_bytes = sizeof(float) * TM * I;
-    unsigned char *ring = smem + 256 + ((h_bytes + 127) / 128) * 128;
-    const size_t rb = row_bytes<FP4>(I);
-    const size_t stage_bytes = kDnRowsPerStage * rb;
+    unsigned char *ring = smem + 512;
+    const uint32_t rb = (uint32_t)row_bytes<FP4>(I);
+    const uint32_t stage_bytes = kDnRows * rb;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], 1);
         }
         *abort_flag = 0;
         fence_barrier_init();
     }
     __syncthreads();
+    grid_dep_launch();
 
-    const long long G = (long long)a.ws.ctrl->n_uniq * d;
-    const long long g_begin = (long long)blockIdx.x * G / gridDim.x;
-    const long long g_end = (long long)(blockIdx.x + 1) * G / gridDim.x;
+    // The routing records come from the kernel before the previous one, which
+    // completed before the previous kernel started: the weight stream may
+    // begin at once. Only h (from the previous kernel) needs the wait below.
+    const int units = a.ws.ctrl->n_uniq * (d / kDnRows);
+    const int u_begin = (int)((long long)blockIdx.x * units / gridDim.x);
+    const int n_st = (int)((long long)(blockIdx.x + 1) * units / gridDim.x) - u_begin;
 
     if (warp == kConsumerWarps) {
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            StageCursor cur{g_begin, g_end, d, kDnRowsPerStage};
             int s = 0;
-            bool ok = true;
-            while (cur.g < cur.end && ok) {
+            for (; s < n_st; ++s) {
                 const int slot = s % NS;
-                if (s >= NS) ok = mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag);
-                if (!ok) break;
-                const int n = cur.next_len();
-                const int u = (int)(cur.g / d), c0 = (int)(cur.g % d);
-                const int e = a.ws.uniq[u];
+                if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
+                const int g = (u_begin + s) * kDnRows;
+                const int u = g / d, c0 = g - u * d;
+                const size_t row = (size_t)a.ws.uniq[u] * d + c0;
                 unsigned char *dst = ring + (size_t)slot * stage_bytes;
-                const size_t row0 = (size_t)e * d + c0;
+                mbar_arrive_expect_tx(&full[slot], stage_bytes);
                 if (!FP4) {
-                    mbar_arrive_expect_tx(&full[slot], (uint32_t)(n * rb));
-                    bulk_g2s(dst, a.wd + row0 * I, (uint32_t)(n * rb), &full[slot], pol);
+                    bulk_g2s(dst, a.wd + row * I, stage_bytes, &full[slot], pol);
                 } else {
-                    const uint32_t nq = (uint32_t)(n * (I / 2)), ns_ = (uint32_t)(n * (I / 16));
-                    mbar_arrive_expect_tx(&full[slot], nq + ns_);
-                    bulk_g2s(dst, a.qd + row0 * (I / 2), nq, &full[slot], pol);
-                    bulk_g2s(dst + kDnRowsPerStage * (I / 2), a.sd + row0 * (I / 16), ns_, &full[slot], pol);
+                    const uint32_t nq = I / 2, nsb = I / 16;
+                    bulk_g2s(dst, a.qd + row * nq, kDnRows * nq, &full[slot], pol);
+                    bulk_g2s(dst + kDnRows * nq, a.sd + row * nsb, kDnRows * nsb, &full[slot], pol);
                 }
-                cur.g += n;
-                ++s;
             }
             for (int j = (s > NS ? s - NS : 0); j < s; ++j) mbar_wait(&full[j % NS], (j / NS) & 1, err);
         }
         return;
     }
 
-    StageCursor cur{g_begin, g_end, d, kDnRowsPerStage};
-    int s = 0;
-    int seg_u = -1, n_e = 0, row_base = 0, e = 0;
-    float gscale = 1.f;
-    while (cur.g < cur.end) {
+    if (warp >= a.ncons) return;
+    grid_dep_wait();      // h from the gate/up kernel
+    ExpertSeg<TM> seg;
+    for (int s = warp; s < n_st; s += a.ncons) {
         const int slot = s % NS;
-        const int n = cur.next_len();
-        const int u = (int)(cur.g / d), c0 = (int)(cur.g % d);
-        if (u != seg_u) {
-            // new expert: reload its h rows into shared memory
-            named_bar(1, 32 * kConsumerWarps);
-            seg_u = u;
-            e = a.ws.uniq[u];
-            n_e = a.ws.counts[e];
-            row_base = a.ws.offsets[e];
-            if (n_e > TM) {
-                atomicOr(err, ERRBIT_RANGE);
-                n_e = TM;
-            }
-            if (FP4) gscale = a.gd[e];
-            const float4 *src = reinterpret_cast<const float4 *>(a.ws.h + (size_t)row_base * I);
-            float4 *dst = reinterpret_cast<float4 *>(hs);
-            for (int i = tid; i < n_e * I / 4; i += 32 * kConsumerWarps) dst[i] = __ldcg(src + i);
-            named_bar(1, 32 * kConsumerWarps);
-        }
-        const bool ok = mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag);
+        const int g = (u_begin + s) * kDnRows;
+        const int u = g / d, c0 = g - u * d;
+        if (u != seg.u) seg.load(a.ws, u, err);
+        if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) return;
         const unsigned char *st = ring + (size_t)slot * stage_bytes;
-        float acc[TM];
+        const float *hrow = a.ws.h + (size_t)seg.row_base * I;
+        float acc[kDnRows][TM];
 #pragma unroll
-        for (int r = 0; r < TM; ++r) acc[r] = 0.f;
-        if (ok && warp < n) {
-            if (!FP4) {
-                const uint4 *wrow = reinterpret_cast<const uint4 *>(st + warp * rb);
-                for (int v = lane; v < I / 8; v += 32) {
-                    float wf[8];
-                    unpack8(wrow[v], wf);
+        for (int q = 0; q < kDnRows; ++q)
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < n_e) {
-                            const float4 *hp = reinterpret_cast<const float4 *>(hs + (size_t)r * I + v * 8);
-                            float4 h0 = hp[0], h1 = hp[1];
-                            float t = wf[0] * h0.x;
-                            t = fmaf(wf[1], h0.y, t);
-                            t = fmaf(wf[2], h0.z, t);
-                            t = fmaf(wf[3], h0.w, t);
-                            t = fmaf(wf[4], h1.x, t);
-                            t = fmaf(wf[5], h1.y, t);
-                            t = fmaf(wf[6], h1.z, t);
-                            t = fmaf(wf[7], h1.w, t);
-                            acc[r] += t;
-                        }
+            for (int r = 0; r < TM; ++r) acc[q][r] = 0.f;
+        if (!FP4) {
+            for (int v = lane; v < I / 8; v += 32) {
+                float wf[kDnRows][8];
+#pragma unroll
+                for (int q = 0; q < kDnRows; ++q) unpack8(reinterpret_cast<const uint4 *>(st + q * rb)[v], wf[q]);
+#pragma unroll
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + v * 8);
+                        const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1);
+#pragma unroll
+                        for (int q = 0; q < kDnRows; ++q) acc[q][r] += dot8h(wf[q], h0, h1);
                     }
                 }
-            } else {
-                const unsigned char *q = st + (size_t)warp * (I / 2);
-                const unsigned char *sc = st + kDnRowsPerStage * (I / 2) + (size_t)warp * (I / 16);
-                for (int b = lane; b < I / 16; b += 32) {
-                    float wf[16];
-                    unpack_fp4x16(*reinterpret_cast<const uint2 *>(q + b * 8), wf);
-                    const float sb = e4m3_to_f32(sc[b]);
+            }
+        } else {
+            const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
+            for (int b = lane; b < I / 16; b += 32) {
+                float wf[kDnRows][16], sc[kDnRows];
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < n_e) {
-                            const float4 *hp = reinterpret_cast<const float4 *>(hs + (size_t)r * I + b * 16);
-                            float t = 0.f;
+                for (int q = 0; q < kDnRows; ++q) {
+                    unpack_fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + b * 8), wf[q]);
+                    sc[q] = e4m3_to_f32(sb[q * (I / 16) + b]);
+                }
 #pragma unroll
-                            for (int qd = 0; qd < 4; ++qd) {
-                                float4 hv = hp[qd];
-                                t = fmaf(wf[4 * qd + 0], hv.x, t);
-                                t = fmaf(wf[4 * qd + 1], hv.y, t);
-                                t = fmaf(wf[4 * qd + 2], hv.z, t);
-                                t = fmaf(wf[4 * qd + 3], hv.w, t);
-                            }
-                            acc[r] = fmaf(t, sb, acc[r]);
-                        }
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + b * 16);
+                        const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1), h2 = __ldcg(hp + 2), h3 = __ldcg(hp + 3);
+#pragma unroll
+                        for (int q = 0; q < kDnRows; ++q)
+                            acc[q][r] = fmaf(dot8h(wf[q], h0, h1) + dot8h(wf[q] + 8, h2, h3), sc[q], acc[q][r]);
                     }
                 }
             }
         }
         __syncwarp();
-        if (lane == 0 && ok) mbar_arrive(&empty[slot]);
-        named_bar(1, 32 * kConsumerWarps);
-        if (*abort_flag) return;
-        if (warp < n) {
+        if (lane == 0) mbar_arrive(&empty[slot]);
+        const float gsc = FP4 ? a.gd[seg.e] : 1.f;
+#pragma unroll
+        for (int q = 0; q < kDnRows; ++q) {
+            float yv = 0.f;
 #pragma unroll
             for (int r = 0; r < TM; ++r) {
-                if (r < n_e) {
-                    float sum = warp_sum(acc[r]);
-                    if (lane == r) a.ws.Y[(size_t)(row_base + r) * d + c0 + warp] = sum * gscale;
+                if (r < seg.n_e) {
+                    const float sum = warp_sum(acc[q][r]);
+                    if (lane == r) yv = sum * gsc;
                 }
             }
+            if (lane < seg.n_e) a.ws.Y[(size_t)(seg.row_base + lane) * d + c0 + q] = yv;
         }
-        cur.g += n;
-        ++s;
     }
 }
 
 // ---------------------------------------------------------------------------
-// launch
+// launch (programmatic dependent launches on the caller's stream)
 // ---------------------------------------------------------------------------
+template <typename K>
+static cudaError_t launch_pdl(K kern, int grid, int threads, size_t smem, cudaStream_t st, const DecodeArgs &a) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+// Ring shape from the number of stages that fit: the most consumer warps c
+// (<= 8) that still own at least two slots each, nstages = c * slots.
+static void pick_stages(int fit, DecodeArgs &a) {
+    if (fit > kMaxStages) fit = kMaxStages;
+    for (int c = kConsumerWarps; c >= 1; --c) {
+        if (fit / c >= 2) {
+            a.ncons = c;
+            a.nstages = (fit / c) * c;
+            return;
+        }
+    }
+    a.ncons = 1;
+    a.nstages = fit;
+}
+
 template <int TM, bool FP4>
 static cudaError_t launch_gateup_t(const LayerDev &L, const DecodeArgs &a0, cudaStream_t st) {
     DecodeArgs a = a0;
-    constexpr int kParts = kConsumerWarps / kGuRowsPerStage;
-    size_t red_bytes = sizeof(float) * 2 * kGuRowsPerStage * kParts * TM * 2;
-    size_t fixed = 256 + align_up(red_bytes, 128) + align_up((size_t)a.T * L.d * 2, 128);
-    size_t stage = 2 * kGuRowsPerStage * row_bytes<FP4>(L.d);
+    const size_t fixed = 512 + align_up((size_t)a.T * L.d * 2, 128);
+    const size_t stage = 2 * row_bytes<FP4>(L.d);
     if (fixed + 2 * stage > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
-    int ns = (int)((kSmemBudget - fixed) / stage);
-    a.nstages = ns > kMaxStages ? kMaxStages : ns;
-    size_t smem = fixed + (size_t)a.nstages * stage;
+    const int ns = (int)((kSmemBudget - fixed) / stage);
+    pick_stages(ns, a);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel<TM, FP4>,
@@ -481,19 +450,18 @@ static cudaError_t launch_gateup_t(const LayerDev &L, const DecodeArgs &a0, cuda
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    decode_gateup_kernel<TM, FP4><<<L.num_sms, kDecodeThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_gateup_kernel<TM, FP4>, L.num_sms, kDecodeThreads, fixed + (size_t)a.nstages * stage,
+                      st, a);
 }
 
 template <int TM, bool FP4>
 static cudaError_t launch_down_t(const LayerDev &L, const DecodeArgs &a0, cudaStream_t st) {
     DecodeArgs a = a0;
-    size_t fixed = 256 + align_up(sizeof(float) * TM * L.I, 128);
-    size_t stage = kDnRowsPerStage * row_bytes<FP4>(L.I);
+    const size_t fixed = 512;
+    const size_t stage = kDnRows * row_bytes<FP4>(L.I);
     if (fixed + 2 * stage > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
-    int ns = (int)((kSmemBudget - fixed) / stage);
-    a.nstages = ns > kMaxStages ? kMaxStages : ns;
-    size_t smem = fixed + (size_t)a.nstages * stage;
+    const int ns = (int)((kSmemBudget - fixed) / stage);
+    pick_stages(ns, a);
     static bool attr = false;
     if (!attr) {
         cudaError_t e = cudaFuncSetAttribute(decode_down_kernel<TM, FP4>,
@@ -501,8 +469,8 @@ static cudaError_t launch_down_t(const LayerDev &L, const DecodeArgs &a0, cudaSt
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    decode_down_kernel<TM, FP4><<<L.num_sms, kDecodeThreads, smem, st>>>(a);
-    return cudaGetLastError();
+    return launch_pdl(decode_down_kernel<TM, FP4>, L.num_sms, kDecodeThreads, fixed + (size_t)a.nstages * stage, st,
+                      a);
 }
 
 template <bool FP4, bool DOWN>
@@ -520,7 +488,7 @@ static cudaError_t launch_fmt(const LayerDev &L, const DecodeArgs &a, cudaStream
 
 static DecodeArgs make_args(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T) {
     return DecodeArgs{x, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd,
-                      T, L.d, L.I, L.k, 0, ws};
+                      T, L.d, L.I, L.k, 0, 0, ws};
 }
 
 cudaError_t launch_decode_gateup(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st) {

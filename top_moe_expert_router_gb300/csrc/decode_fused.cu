@@ -1,0 +1,780 @@
+// decode_fused.cu — one persistent kernel for a whole small-batch (T <= 16)
+// MoE layer: router, softmax/top-k/renormalise, permutation, the expert
+// weight stream through gate/up and down, and the weighted combine.
+//
+// Decode is bound by streaming weights from HBM and by the boundaries
+// between kernels, which break the overlap of weight streaming and compute
+// ("How SGLang-TorchTPU accelerated an 816B-parameter MoE on TPU v7",
+// sections "Introduction" and "Key optimisations"). Here the layer is one
+// cooperative launch, one CTA per SM:
+//   1. router: every CTA computes the logits of its experts (x . Wr[e]),
+//      grid barrier;
+//   2. routing: every CTA computes top-k and the permutation of all T tokens
+//      itself, in shared memory (identical results everywhere; CTA 0 also
+//      publishes them), so no second barrier is needed;
+//   3. one producer lane fills a ring of shared-memory slots with bulk TMA
+//      copies: first this CTA's share of the active experts' gate/up rows,
+//      then, without a pause, its share of their down rows; slot j belongs
+//      to consumer warp j % c, which takes the slot's phases in order;
+//   4. consumer warps compute h = silu(Wg x) * (Wu x) (fp32, to global), meet
+//      at a grid barrier (all of h written) while the producer keeps
+//      fetching down rows, then compute Y = Wd h (fp32, to global);
+//   5. combine: per 256-column block of the output, the CTA whose down rows
+//      complete the block (a row counter per block) forms
+//      out = (res +) sum_j w_j Y_j for those columns, in fp32, j ascending.
+// Every wait (mbarrier, grid barrier) is bounded; a timeout sets the error
+// word and the kernel unwinds.
+#include <cuda_fp4.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include "common.cuh"
+
+namespace moe {
+
+namespace fused {
+
+constexpr int kConsumers = 8;                 // consumer warps at most
+constexpr int kThreads = 32 * (kConsumers + 1);
+constexpr int kProducerWarp = kConsumers;
+constexpr int kDnRows = 4;                    // down rows per stage
+constexpr int kMaxSlots = 32;
+constexpr int kSmemBudget = 227 * 1024;
+constexpr int kCb = 256;                      // output columns per combine block
+
+struct Args {
+    const uint16_t *x;        // [T, d] bf16
+    const uint16_t *res;      // [T, d] bf16 or null
+    uint16_t *out;            // [T, d] bf16
+    const uint16_t *wr;       // [E, d]
+    const float *bias;        // [E] or null
+    const uint16_t *wg, *wu, *wd;
+    const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
+    const float *gg, *gu, *gd;
+    int T, d, I, E, k;
+    int nslots, ncons;
+    uint32_t slot_bytes;
+    int x_in_smem;            // tokens' rows staged in shared memory
+    int do_combine;           // 0: leave Y for a separate combine kernel
+    Workspace ws;
+};
+
+template <bool FP4>
+__host__ __device__ constexpr uint32_t rowb(int K) {
+    return FP4 ? (uint32_t)K / 2 + (uint32_t)K / 16 : (uint32_t)K * 2;
+}
+
+// ---------------------------------------------------------------------------
+// small helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
+
+__device__ __forceinline__ void fp4x16(uint2 q, float2 f[8]) {
+    const uint32_t words[2] = {q.x, q.y};
+#pragma unroll
+    for (int wi = 0; wi < 2; ++wi)
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((words[wi] >> (8 * b)) & 0xFFu),
+                                                       __NV_E2M1);
+            f[wi * 4 + b] = __half22float2(*reinterpret_cast<__half2 *>(&hr));
+        }
+}
+
+__device__ __forceinline__ float e4m3f(uint8_t s) {
+    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)s, __NV_E4M3);
+    return __half2float(*reinterpret_cast<__half *>(&hr));
+}
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Grid barrier over all CTAs of the (cooperative) launch: arrival counter
+// `target` = (barrier index) x (grid size). Bounded wait.
+__device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, volatile int *abort_flag) {
+    __syncthreads();
+    __shared__ int ok;
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        ok = 1;
+        unsigned long long t0 = global_ns();
+        while (ld_acquire(ctr) < target) {
+            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(err, ERRBIT_TIMEOUT);
+                *abort_flag = 1;
+                ok = 0;
+                break;
+            }
+            __nanosleep(64);
+        }
+        __threadfence();
+    }
+    __syncthreads();
+    return ok != 0;
+}
+
+// Per-warp cache of the expert a stage belongs to (read from shared memory).
+template <int TM>
+struct Seg {
+    int u = -1, e = 0, n_e = 0, row0 = 0;
+    int tok[TM];
+};
+
+// Routing state in shared memory.
+struct Route {
+    int32_t *ids, *pos, *perm, *cnt, *off, *uniq, *scan;
+    float *w;
+    uint32_t *bm;
+    int *n_uniq;
+};
+
+template <int TM>
+__device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
+    s.u = u;
+    s.e = R.uniq[u];
+    s.n_e = R.cnt[s.e] < TM ? R.cnt[s.e] : TM;
+    s.row0 = R.off[s.e];
+#pragma unroll
+    for (int r = 0; r < TM; ++r) s.tok[r] = r < s.n_e ? R.perm[s.row0 + r] : 0;
+}
+
+// top-k of one token by one warp, weights exp(l - lmax) / sum over the kept
+__device__ void topk_to_smem(const float *logits_row, int E, int k, int32_t *ids, float *w) {
+    const int lane = threadIdx.x & 31;
+    float v[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        v[i] = e < E ? __ldcg(logits_row + e) : -INFINITY;
+    }
+    uint32_t taken = 0;
+    float lmax = 0.f, sum = 0.f, my_val = 0.f;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int bi = 0x7FFFFFFF;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
+                bv = v[i];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
+            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (ov > bv || (ov == bv && oi < bi)) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+        if (j == 0) lmax = bv;
+        const float ex = expf(bv - lmax);
+        sum += ex;
+        if (lane == j) {
+            my_val = ex;
+            my_id = bi;
+        }
+    }
+    if (lane < k) {
+        ids[lane] = my_id;
+        w[lane] = my_val / sum;
+    }
+}
+
+// exclusive scan of a[0..n) (n <= 256) by one warp; returns the total
+__device__ int warp_scan256(const int32_t *a, int32_t *out, int n) {
+    const int lane = threadIdx.x & 31;
+    int vals[8], local = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        vals[i] = idx < n ? a[idx] : 0;
+        local += vals[i];
+    }
+    int incl = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+        if (lane >= o) incl += y;
+    }
+    int run = incl - local;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int idx = lane * 8 + i;
+        if (idx < n) out[idx] = run;
+        run += vals[i];
+    }
+    return __shfl_sync(0xFFFFFFFFu, incl, 31);
+}
+
+// ---------------------------------------------------------------------------
+// the kernel
+// ---------------------------------------------------------------------------
+template <int TM, bool FP4>
+__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int d = a.d, I = a.I, E = a.E, k = a.k, T = a.T, NS = a.nslots, C = a.ncons;
+    const int G = gridDim.x, b = blockIdx.x;
+    uint32_t *err = &a.ws.ctrl->err;
+    Control *ctrl = a.ws.ctrl;
+
+    // ---- shared-memory layout ----
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
+    uint64_t *empty = full + kMaxSlots;
+    uint64_t *xbar = empty + kMaxSlots;             // bytes [512, 520)
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 520);
+    int *n_uniq_s = reinterpret_cast<int *>(smem + 524);
+    int *cb_rows_s = reinterpret_cast<int *>(smem + 528);   // [32]
+    int *cb_todo = cb_rows_s + 32;                  // [32]
+    int *n_todo = cb_todo + 32;
+    float *part = reinterpret_cast<float *>(smem + 1024);   // [8 warps][TM] router partials
+    unsigned char *rbase = smem + 2048;             // routing scratch (8 KB)
+    Route R;
+    R.cnt = reinterpret_cast<int32_t *>(rbase);     // [257]
+    R.off = R.cnt + 260;                            // [257]
+    R.uniq = R.off + 260;                           // [256]
+    R.scan = R.uniq + 260;                          // [257]
+    R.bm = reinterpret_cast<uint32_t *>(R.scan + 260);      // [256]
+    R.ids = reinterpret_cast<int32_t *>(R.bm + 256);        // [16 * 8]
+    R.pos = R.ids + 128;                            // [16 * 8]
+    R.perm = R.pos + 128;                           // [16 * 8]
+    R.w = reinterpret_cast<float *>(R.perm + 128);  // [16 * 8]
+    R.n_uniq = n_uniq_s;
+    unsigned char *xs = smem + 2048 + 8192;
+    const uint32_t x_bytes = a.x_in_smem ? (uint32_t)T * d * 2 : 0u;
+    unsigned char *ring = xs + ((x_bytes + 127) / 128) * 128;
+
+    if (tid == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(xbar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    for (int i = tid; i < 32; i += kThreads) cb_rows_s[i] = 0;
+    __syncthreads();
+    if (tid == 32 * kProducerWarp && x_bytes) {
+        mbar_arrive_expect_tx(xbar, x_bytes);
+        bulk_g2s(xs, a.x, x_bytes, xbar, policy_evict_last());
+    }
+
+    // ---- 1. router: logits of this CTA's experts ----
+    // experts b, b + G, b + 2G, ... two at a time: warps 0-3 / 4-7 take the
+    // four quarters of one expert's row
+    if (x_bytes && !mbar_wait_or_abort(xbar, 0, err, abort_flag)) {
+        // fall through: the grid barrier below reports and unwinds
+    }
+    {
+        const int nq = d / 32;  // 16-byte vectors per quarter row
+        for (int base = b; base < E; base += 2 * G) {
+            const int eidx = base + (warp >= 4 ? G : 0);
+            const int q = warp & 3;
+            float acc[TM];
+#pragma unroll
+            for (int t = 0; t < TM; ++t) acc[t] = 0.f;
+            if (warp < 8 && eidx < E) {
+                const uint4 *wrow = reinterpret_cast<const uint4 *>(a.wr + (size_t)eidx * d) + q * nq;
+                for (int v = lane; v < nq; v += 32) {
+                    const uint4 wv = __ldg(wrow + v);
+#pragma unroll
+                    for (int t = 0; t < TM; ++t) {
+                        if (t < T) {
+                            const uint4 xv = a.x_in_smem
+                                                 ? reinterpret_cast<const uint4 *>(xs + (size_t)t * d * 2)[q * nq + v]
+                                                 : __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * d) + q * nq + v);
+                            float2 s2 = make_float2(0.f, 0.f);
+                            s2 = ffma2(bf2(wv.x), bf2(xv.x), s2);
+                            s2 = ffma2(bf2(wv.y), bf2(xv.y), s2);
+                            s2 = ffma2(bf2(wv.z), bf2(xv.z), s2);
+                            s2 = ffma2(bf2(wv.w), bf2(xv.w), s2);
+                            acc[t] += s2.x + s2.y;
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int t = 0; t < TM; ++t) {
+                const float s = warp_sum(acc[t]);
+                if (lane == 0 && warp < 8) part[warp * TM + t] = s;
+            }
+            __syncthreads();
+            if (tid < 2 * TM) {
+                const int half = tid / TM, t = tid % TM;
+                const int e2 = base + half * G;
+                if (e2 < E && t < T) {
+                    const float *pp = part + half * 4 * TM;
+                    float l = ((pp[0 * TM + t] + pp[1 * TM + t]) + pp[2 * TM + t]) + pp[3 * TM + t];
+                    if (a.bias) l += a.bias[e2];
+                    a.ws.logits[(size_t)t * E + e2] = l;
+                }
+            }
+            __syncthreads();
+        }
+    }
+    grid_barrier(&ctrl->grid_bar, (uint32_t)G, err, abort_flag);
+
+    // ---- 2. routing, computed by every CTA in shared memory ----
+    for (int t = warp; t < T; t += kConsumers + 1)
+        topk_to_smem(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k);
+    for (int e = tid; e < E; e += kThreads) R.bm[e] = 0u;
+    __syncthreads();
+    for (int p = tid; p < T * k; p += kThreads) {
+        const int e = R.ids[p];
+        if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += kThreads) {
+        const int c = __popc(R.bm[e]);
+        R.cnt[e] = c;
+        R.scan[e] = c > 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int total = warp_scan256(R.cnt, R.off, E);
+        __syncwarp();
+        const int nu = warp_scan256(R.scan, R.scan, E);
+        __syncwarp();
+        for (int e = lane; e < E; e += 32)
+            if (R.cnt[e] > 0) R.uniq[R.scan[e]] = e;
+        if (lane == 0) {
+            R.off[E] = total;
+            *R.n_uniq = nu;
+        }
+    }
+    __syncthreads();
+    for (int p = tid; p < T * k; p += kThreads) {
+        const int e = R.ids[p];
+        const int t = p / k;
+        const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
+        R.perm[row] = t;
+        R.pos[p] = row;
+    }
+    __syncthreads();
+    const int n_uniq = *R.n_uniq;
+    if (b == 0) {  // publish the routing records
+        for (int p = tid; p < T * k; p += kThreads) {
+            a.ws.ids[p] = R.ids[p];
+            a.ws.w[p] = R.w[p];
+            a.ws.pos[p] = R.pos[p];
+            a.ws.perm[p] = R.perm[p];
+        }
+        for (int e = tid; e < E; e += kThreads) {
+            a.ws.counts[e] = R.cnt[e];
+            a.ws.offsets[e] = R.off[e];
+            a.ws.tile_off[e] = 0;
+        }
+        for (int u = tid; u < n_uniq; u += kThreads) a.ws.uniq[u] = R.uniq[u];
+        if (tid == 0) {
+            a.ws.offsets[E] = R.off[E];
+            a.ws.tile_off[E] = 0;
+            ctrl->n_uniq = n_uniq;
+        }
+    }
+
+    // ---- 3./4. the weight stream ----
+    const int gu_total = n_uniq * I;
+    const int gu_b = (int)((long long)b * gu_total / G);
+    const int n_gu = (int)((long long)(b + 1) * gu_total / G) - gu_b;
+    const int dn_total = n_uniq * (d / kDnRows);
+    const int dn_b = (int)((long long)b * dn_total / G);
+    const int n_dn = (int)((long long)(b + 1) * dn_total / G) - dn_b;
+    const int n_st = n_gu + n_dn;
+    const uint32_t rbg = rowb<FP4>(d), rbd = rowb<FP4>(I);
+
+    if (warp == kProducerWarp) {
+        if (lane == 0 && !*abort_flag) {
+            const uint64_t pol = policy_evict_first();
+            int s = 0;
+            for (; s < n_st; ++s) {
+                const int slot = s % NS;
+                if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
+                unsigned char *dst = ring + (size_t)slot * a.slot_bytes;
+                if (s < n_gu) {
+                    const int g = gu_b + s;
+                    const int u = g / I, i = g - u * I;
+                    const size_t row = (size_t)R.uniq[u] * I + i;
+                    mbar_arrive_expect_tx(&full[slot], 2 * rbg);
+                    if (!FP4) {
+                        bulk_g2s(dst, a.wg + row * d, rbg, &full[slot], pol);
+                        bulk_g2s(dst + rbg, a.wu + row * d, rbg, &full[slot], pol);
+                    } else {
+                        const uint32_t nq = d / 2, nsb = d / 16;
+                        bulk_g2s(dst, a.qg + row * nq, nq, &full[slot], pol);
+                        bulk_g2s(dst + nq, a.sg + row * nsb, nsb, &full[slot], pol);
+                        bulk_g2s(dst + rbg, a.qu + row * nq, nq, &full[slot], pol);
+                        bulk_g2s(dst + rbg + nq, a.su + row * nsb, nsb, &full[slot], pol);
+                    }
+                } else {
+                    const int g = (dn_b + (s - n_gu)) * kDnRows;
+                    const int u = g / d, c0 = g - u * d;
+                    const size_t row = (size_t)R.uniq[u] * d + c0;
+                    mbar_arrive_expect_tx(&full[slot], kDnRows * rbd);
+                    if (!FP4) {
+                        bulk_g2s(dst, a.wd + row * I, kDnRows * rbd, &full[slot], pol);
+                    } else {
+                        const uint32_t nq = I / 2, nsb = I / 16;
+                        bulk_g2s(dst, a.qd + row * nq, kDnRows * nq, &full[slot], pol);
+                        bulk_g2s(dst + kDnRows * nq, a.sd + row * nsb, kDnRows * nsb, &full[slot], pol);
+                    }
+                }
+            }
+            // every copy issued must land before the CTA moves on
+            for (int j = (s > NS ? s - NS : 0); j < s; ++j) mbar_wait(&full[j % NS], (j / NS) & 1, err);
+        }
+    } else if (warp < C) {
+        // ------------------------------- gate/up -------------------------------
+        Seg<TM> seg;
+        int s = warp;
+        for (; s < n_gu && !*abort_flag; s += C) {
+            const int slot = s % NS;
+            const int g = gu_b + s;
+            const int u = g / I, i = g - u * I;
+            if (u != seg.u) seg_load(seg, R, u);
+            if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
+            const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
+            float2 ag[TM], au[TM];
+#pragma unroll
+            for (int r = 0; r < TM; ++r) ag[r] = au[r] = make_float2(0.f, 0.f);
+            if (!FP4) {
+                const uint4 *gw = reinterpret_cast<const uint4 *>(st);
+                const uint4 *uw = reinterpret_cast<const uint4 *>(st + rbg);
+#pragma unroll 2
+                for (int v = lane; v < d / 8; v += 32) {
+                    const uint4 g4 = gw[v], u4 = uw[v];
+                    const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
+                    const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
+#pragma unroll
+                    for (int r = 0; r < TM; ++r) {
+                        if (r < seg.n_e) {
+                            const uint4 xv =
+                                a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v]
+                                            : __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + v);
+                            const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
+                            ag[r] = ffma2(g0, x0, ag[r]);
+                            au[r] = ffma2(u0, x0, au[r]);
+                            ag[r] = ffma2(g1, x1, ag[r]);
+                            au[r] = ffma2(u1, x1, au[r]);
+                            ag[r] = ffma2(g2, x2, ag[r]);
+                            au[r] = ffma2(u2, x2, au[r]);
+                            ag[r] = ffma2(g3, x3, ag[r]);
+                            au[r] = ffma2(u3, x3, au[r]);
+                        }
+                    }
+                }
+            } else {
+                const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rbg, *us = st + rbg + d / 2;
+                for (int bb = lane; bb < d / 16; bb += 32) {
+                    float2 gf[8], uf[8];
+                    fp4x16(*reinterpret_cast<const uint2 *>(gq + bb * 8), gf);
+                    fp4x16(*reinterpret_cast<const uint2 *>(uq + bb * 8), uf);
+                    const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
+#pragma unroll
+                    for (int r = 0; r < TM; ++r) {
+                        if (r < seg.n_e) {
+                            const uint4 *xp =
+                                a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2
+                                            : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + bb * 2;
+                            const uint4 xa = a.x_in_smem ? xp[0] : __ldg(xp), xb = a.x_in_smem ? xp[1] : __ldg(xp + 1);
+                            const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                            float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float2 xq = bf2(xw[q]);
+                                pg = ffma2(gf[q], xq, pg);
+                                pu = ffma2(uf[q], xq, pu);
+                            }
+                            ag[r].x = fmaf(pg.x + pg.y, sgb, ag[r].x);
+                            au[r].x = fmaf(pu.x + pu.y, sub, au[r].x);
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
+            float hv = 0.f;
+#pragma unroll
+            for (int r = 0; r < TM; ++r) {
+                if (r < seg.n_e) {
+                    const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
+                    const float su_ = warp_sum(au[r].x + au[r].y) * usc;
+                    if (lane == r) hv = silu(sg_) * su_;
+                }
+            }
+            if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
+        }
+        // all consumer warps of every CTA have written their h: grid barrier
+        named_bar(1, 32 * C);
+        if (warp == 0 && lane == 0) {
+            __threadfence();
+            atomicAdd(&ctrl->grid_bar, 1u);
+            const unsigned long long t0 = global_ns();
+            while (ld_acquire(&ctrl->grid_bar) < 2u * G) {
+                if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                    atomicOr(err, ERRBIT_TIMEOUT);
+                    *abort_flag = 1;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            __threadfence();
+        }
+        named_bar(1, 32 * C);
+        // ---------------------------------- down ----------------------------------
+        Seg<TM> sd;
+        for (; s < n_st && !*abort_flag; s += C) {
+            const int slot = s % NS;
+            const int g = (dn_b + (s - n_gu)) * kDnRows;
+            const int u = g / d, c0 = g - u * d;
+            if (u != sd.u) seg_load(sd, R, u);
+            if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
+            const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
+            const float *hrow = a.ws.h + (size_t)sd.row0 * I;
+            float2 acc[kDnRows][TM];
+#pragma unroll
+            for (int q = 0; q < kDnRows; ++q)
+#pragma unroll
+                for (int r = 0; r < TM; ++r) acc[q][r] = make_float2(0.f, 0.f);
+            if (!FP4) {
+                for (int v = lane; v < I / 8; v += 32) {
+                    uint4 wv[kDnRows];
+#pragma unroll
+                    for (int q = 0; q < kDnRows; ++q) wv[q] = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+#pragma unroll
+                    for (int r = 0; r < TM; ++r) {
+                        if (r < sd.n_e) {
+                            const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + v * 8);
+                            const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1);
+                            const float2 ha = make_float2(h0.x, h0.y), hb = make_float2(h0.z, h0.w);
+                            const float2 hc = make_float2(h1.x, h1.y), hd = make_float2(h1.z, h1.w);
+#pragma unroll
+                            for (int q = 0; q < kDnRows; ++q) {
+                                acc[q][r] = ffma2(bf2(wv[q].x), ha, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv[q].y), hb, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv[q].z), hc, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv[q].w), hd, acc[q][r]);
+                            }
+                        }
+                    }
+                }
+            } else {
+                const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
+                for (int bb = lane; bb < I / 16; bb += 32) {
+#pragma unroll
+                    for (int q = 0; q < kDnRows; ++q) {
+                        float2 wf[8];
+                        fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
+                        const float sc = e4m3f(sb[q * (I / 16) + bb]);
+#pragma unroll
+                        for (int r = 0; r < TM; ++r) {
+                            if (r < sd.n_e) {
+                                const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + bb * 16);
+                                float2 p = make_float2(0.f, 0.f);
+#pragma unroll
+                                for (int h4 = 0; h4 < 4; ++h4) {
+                                    const float4 hv = __ldcg(hp + h4);
+                                    p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
+                                    p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
+                                }
+                                acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
+                            }
+                        }
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+            const float gsc = FP4 ? a.gd[sd.e] : 1.f;
+#pragma unroll
+            for (int q = 0; q < kDnRows; ++q) {
+                float yv = 0.f;
+#pragma unroll
+                for (int r = 0; r < TM; ++r) {
+                    if (r < sd.n_e) {
+                        const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
+                        if (lane == r) yv = sum * gsc;
+                    }
+                }
+                if (lane < sd.n_e) a.ws.Y[(size_t)(sd.row0 + lane) * d + c0 + q] = yv;
+            }
+            if (lane == 0) atomicAdd(&cb_rows_s[c0 / kCb], kDnRows);
+        }
+    }
+
+    // ---- 5. combine, by the CTA that completes each column block ----
+    __threadfence();  // this thread's h and Y stores before the block's count below
+    __syncthreads();
+    if (a.do_combine) {
+        if (tid == 0) {
+            int n = 0;
+            __threadfence();
+            const int ncb = (d + kCb - 1) / kCb;
+            for (int cb = 0; cb < ncb; ++cb) {
+                const int mine = cb_rows_s[cb];
+                if (!mine) continue;
+                const int cols = min(kCb, d - cb * kCb);
+                const uint32_t done = atomicAdd(&ctrl->cb_rows[cb], (uint32_t)mine) + mine;
+                if (done == (uint32_t)(n_uniq * cols)) cb_todo[n++] = cb;
+            }
+            *n_todo = n;
+            __threadfence();
+        }
+        __syncthreads();
+        for (int ti = 0; ti < *n_todo; ++ti) {
+            const int cb = cb_todo[ti];
+            const int cols = min(kCb, d - cb * kCb);
+            for (int idx = tid; idx < T * (cols / 4); idx += kThreads) {
+                const int t = idx / (cols / 4);
+                const int c = cb * kCb + (idx % (cols / 4)) * 4;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int j = 0; j < k; ++j) {
+                    const float wj = R.w[t * k + j];
+                    const float4 y = __ldcg(reinterpret_cast<const float4 *>(a.ws.Y + (size_t)R.pos[t * k + j] * d + c));
+                    acc.x = fmaf(wj, y.x, acc.x);
+                    acc.y = fmaf(wj, y.y, acc.y);
+                    acc.z = fmaf(wj, y.z, acc.z);
+                    acc.w = fmaf(wj, y.w, acc.w);
+                }
+                if (a.res) {
+                    const uint2 rv = *reinterpret_cast<const uint2 *>(a.res + (size_t)t * d + c);
+                    acc.x += bf16lo(rv.x);
+                    acc.y += bf16hi(rv.x);
+                    acc.z += bf16lo(rv.y);
+                    acc.w += bf16hi(rv.y);
+                }
+                uint2 o;
+                o.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
+                o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
+                *reinterpret_cast<uint2 *>(a.out + (size_t)t * d + c) = o;
+            }
+            if (tid == 0) ctrl->cb_rows[cb] = 0u;
+        }
+    }
+    // ---- exit: the last CTA out resets the grid-barrier counters ----
+    __syncthreads();
+    if (tid == 0) {
+        __threadfence();
+        if (atomicAdd(&ctrl->grid_exit, 1u) == (uint32_t)G - 1) {
+            for (int cb = 0; cb < 32; ++cb) ctrl->cb_rows[cb] = 0u;  // zero already unless a wait gave up
+            ctrl->grid_bar = 0u;
+            ctrl->grid_exit = 0u;
+            __threadfence();
+        }
+    }
+}
+
+template <bool FP4>
+static int pick(int fit, int &ncons) {
+    if (fit > kMaxSlots) fit = kMaxSlots;
+    for (int c = kConsumers; c >= 1; --c)
+        if (fit / c >= 2) {
+            ncons = c;
+            return (fit / c) * c;
+        }
+    ncons = 1;
+    return fit;
+}
+
+template <int TM, bool FP4>
+static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16_t *x, const uint16_t *res,
+                            uint16_t *out, int T, cudaStream_t st) {
+    Args a{};
+    a.x = x;
+    a.res = res;
+    a.out = out;
+    a.wr = L.wr;
+    a.bias = L.bias;
+    a.wg = L.wg;
+    a.wu = L.wu;
+    a.wd = L.wd;
+    a.qg = L.qg;
+    a.qu = L.qu;
+    a.qd = L.qd;
+    a.sg = L.sg;
+    a.su = L.su;
+    a.sd = L.sd;
+    a.gg = L.gg;
+    a.gu = L.gu;
+    a.gd = L.gd;
+    a.T = T;
+    a.d = L.d;
+    a.I = L.I;
+    a.E = L.E;
+    a.k = L.k;
+    a.ws = ws;
+    a.do_combine = L.expert_norm ? 0 : 1;
+    const uint32_t slot = (uint32_t)(2 * rowb<FP4>(L.d) > kDnRows * rowb<FP4>(L.I) ? 2 * rowb<FP4>(L.d)
+                                                                                     : kDnRows * rowb<FP4>(L.I));
+    a.slot_bytes = (slot + 127) / 128 * 128;
+    const size_t fixed = 2048 + 8192;
+    a.x_in_smem = T <= 8 ? 1 : 0;
+    const size_t xb = a.x_in_smem ? align_up((size_t)T * L.d * 2, 128) : 0;
+    if (fixed + xb + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) {
+        a.x_in_smem = 0;
+    }
+    const size_t xb2 = a.x_in_smem ? xb : 0;
+    if (fixed + xb2 + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
+    const int fit = (int)((kSmemBudget - fixed - xb2) / a.slot_bytes);
+    a.nslots = pick<FP4>(fit, a.ncons);
+    const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
+    static bool attr = false;
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<TM, FP4>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(L.num_sms);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attrs[1];
+    attrs[0].id = cudaLaunchAttributeCooperative;
+    attrs[0].val.cooperative = 1;
+    cfg.attrs = attrs;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<TM, FP4>, a);
+}
+
+}  // namespace fused
+
+// Whole small-batch layer in one launch (plus the normalising combine when
+// the layer asks for per-expert output normalisation).
+cudaError_t launch_decode_fused(const LayerDev &L, const Workspace &ws, const uint16_t *x, const uint16_t *res,
+                                uint16_t *out, int T, cudaStream_t st) {
+    using namespace fused;
+    if (L.E > 256 || L.k > 8 || T > 16 || L.d > 32 * kCb) return cudaErrorInvalidValue;
+    cudaError_t e;
+    const bool fp4 = L.fmt == MOE_W_NVFP4;
+#define MOE_FUSED(TMV) e = fp4 ? launch_t<TMV, true>(L, ws, x, res, out, T, st) : launch_t<TMV, false>(L, ws, x, res, out, T, st)
+    if (T <= 1)
+        MOE_FUSED(1);
+    else if (T <= 2)
+        MOE_FUSED(2);
+    else if (T <= 4)
+        MOE_FUSED(4);
+    else if (T <= 8)
+        MOE_FUSED(8);
+    else
+        MOE_FUSED(16);
+#undef MOE_FUSED
+    if (e != cudaSuccess) return e;
+    if (L.expert_norm) e = launch_combine(L, ws, res, out, T, st);
+    return e;
+}
+
+}  // namespace moe

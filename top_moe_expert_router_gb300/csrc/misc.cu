@@ -19,22 +19,38 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
                                                       const int32_t *__restrict__ pos,
                                                       const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
                                                       int T, int d, int k, uint32_t *err, int rows) {
+    // launched as a programmatic dependent: Y, w and pos come from the
+    // kernels before it
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.y;
     const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
     if (c >= d) return;
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = 0; j < k; ++j) {
-        const float wj = w[(size_t)t * k + j];
-        const int r = pos[(size_t)t * k + j];
-        if ((unsigned)r >= (unsigned)rows) {
+    // all slot records first, then all expert-output loads, then the sum
+    float wj[8];
+    int rj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        wj[j] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.f;
+        rj[j] = j < k ? __ldcg(pos + (size_t)t * k + j) : 0;
+        if ((unsigned)rj[j] >= (unsigned)rows) {
             atomicOr(err, ERRBIT_RANGE);
-            continue;
+            rj[j] = 0;
+            wj[j] = 0.f;
         }
-        const float4 y = __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)r * d + c));
-        acc.x = fmaf(wj, y.x, acc.x);
-        acc.y = fmaf(wj, y.y, acc.y);
-        acc.z = fmaf(wj, y.z, acc.z);
-        acc.w = fmaf(wj, y.w, acc.w);
+    }
+    float4 y[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        y[j] = j < k ? __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)rj[j] * d + c)) : make_float4(0, 0, 0, 0);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+            acc.x = fmaf(wj[j], y[j].x, acc.x);
+            acc.y = fmaf(wj[j], y[j].y, acc.y);
+            acc.z = fmaf(wj[j], y[j].z, acc.z);
+            acc.w = fmaf(wj[j], y[j].w, acc.w);
+        }
     }
     if (res) {
         const uint2 rv = *reinterpret_cast<const uint2 *>(res + (size_t)t * d + c);
@@ -49,11 +65,106 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = o;
 }
 
+// With per-expert output normalisation: one CTA per token; pass 1 sums the
+// squares of each slot's expert output over d, pass 2 forms
+// (res +) sum_j w_j * Y_j / sqrt(mean(Y_j^2) + 1e-6) in fp32, j ascending.
+__global__ void __launch_bounds__(256) combine_norm_kernel(const float *__restrict__ Y, const float *__restrict__ w,
+                                                           const int32_t *__restrict__ pos,
+                                                           const uint16_t *__restrict__ res,
+                                                           uint16_t *__restrict__ out, int T, int d, int k,
+                                                           uint32_t *err, int rows) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    __shared__ float part[8][8];
+    __shared__ float fac[8];
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    float wj[8];
+    int rj[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        wj[j] = j < k ? __ldcg(w + (size_t)t * k + j) : 0.f;
+        rj[j] = j < k ? __ldcg(pos + (size_t)t * k + j) : 0;
+        if ((unsigned)rj[j] >= (unsigned)rows) {
+            atomicOr(err, ERRBIT_RANGE);
+            rj[j] = 0;
+            wj[j] = 0.f;
+        }
+    }
+    float ss[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss[j] = 0.f;
+    for (int c = tid * 4; c < d; c += 1024) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < k) {
+                const float4 y = __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)rj[j] * d + c));
+                ss[j] = fmaf(y.x, y.x, fmaf(y.y, y.y, fmaf(y.z, y.z, fmaf(y.w, y.w, ss[j]))));
+            }
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const float s = warp_sum(ss[j]);
+        if (lane == 0) part[warp][j] = s;
+    }
+    __syncthreads();
+    if (tid < 8) {
+        float s = 0.f;
+        for (int i = 0; i < 8; ++i) s += part[i][tid];
+        fac[tid] = 1.0f / sqrtf(s / (float)d + 1e-6f);
+    }
+    __syncthreads();
+    for (int c = tid * 4; c < d; c += 1024) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            if (j < k) {
+                const float4 y = __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)rj[j] * d + c));
+                const float f = fac[j];
+                acc.x = fmaf(wj[j], y.x * f, acc.x);
+                acc.y = fmaf(wj[j], y.y * f, acc.y);
+                acc.z = fmaf(wj[j], y.z * f, acc.z);
+                acc.w = fmaf(wj[j], y.w * f, acc.w);
+            }
+        }
+        if (res) {
+            const uint2 rv = *reinterpret_cast<const uint2 *>(res + (size_t)t * d + c);
+            acc.x += bf16lo(rv.x);
+            acc.y += bf16hi(rv.x);
+            acc.z += bf16lo(rv.y);
+            acc.w += bf16hi(rv.y);
+        }
+        uint2 o;
+        o.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
+        o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
+        *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = o;
+    }
+}
+
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
                            cudaStream_t st) {
-    dim3 grid((L.d / 4 + 255) / 256, T);
-    combine_kernel<<<grid, 256, 0, st>>>(ws.Y, ws.w, ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg{};
+    if (L.expert_norm) {
+        cfg.gridDim = dim3(T);
+        cfg.blockDim = dim3(256);
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, combine_norm_kernel, (const float *)ws.Y, (const float *)ws.w,
+                                  (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
+    }
+    cfg.gridDim = dim3((L.d / 4 + 255) / 256, T);
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)ws.Y, (const float *)ws.w,
+                              (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
 }
 
 // ---------------------------------------------------------------------------

@@ -104,89 +104,55 @@ __device__ int warp0_exclusive_scan(const int32_t *a, int32_t *out, int n, int l
     return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
-__device__ void permute_block(const int32_t *ids, int T, int k, int E, const Workspace &ws, PermSmem sm) {
-    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5, nwarps = nth >> 5;
-    for (int e = tid; e < E; e += nth) sm.cnt[e] = 0;
-    __syncthreads();
+// Permutation for T <= 32 tokens: bm[e] holds one bit per token routed to e,
+// so the row of (t, j) is offsets[e] + popcount(bm[e] below bit t).
+__device__ void permute_block_small(const int32_t *ids, int T, int k, int E, const Workspace &ws, PermSmem sm) {
+    const int tid = threadIdx.x, nth = blockDim.x, lane = tid & 31, warp = tid >> 5;
     const int Tk = T * k;
-    for (int i = tid; i < Tk; i += nth) {
-        int e = ids[i];
+    for (int e = tid; e < E; e += nth) sm.bm[e] = 0u;
+    __syncthreads();
+    for (int p = tid; p < Tk; p += nth) {
+        const int e = ids[p];
         if ((unsigned)e < (unsigned)E)
-            atomicAdd(&sm.cnt[e], 1);
+            atomicOr(&sm.bm[e], 1u << (p / k));
         else
             atomicOr(&ws.ctrl->err, ERRBIT_RANGE);
     }
     __syncthreads();
+    for (int e = tid; e < E; e += nth) {
+        const int c = __popc(sm.bm[e]);
+        sm.cnt[e] = c;
+        sm.scratch[e] = c > 0 ? 1 : 0;
+    }
+    __syncthreads();
     if (warp == 0) {
-        int total = warp0_exclusive_scan(sm.cnt, sm.off, E, lane);
-        if (lane == 0) sm.off[E] = total;
-        // experts with tokens, ascending
-        for (int e = lane; e < E; e += 32) sm.scratch[e] = sm.cnt[e] > 0 ? 1 : 0;
-        __syncwarp();
-        int nu = warp0_exclusive_scan(sm.scratch, sm.run, E, lane);
+        const int total = warp0_exclusive_scan(sm.cnt, sm.off, E, lane);
+        const int nu = warp0_exclusive_scan(sm.scratch, sm.run, E, lane);
         __syncwarp();
         for (int e = lane; e < E; e += 32)
             if (sm.cnt[e] > 0) ws.uniq[sm.run[e]] = e;
-        // 128-row tiles per expert (prefill grouped GEMM)
-        for (int e = lane; e < E; e += 32) sm.scratch[e] = (sm.cnt[e] + 127) >> 7;
-        __syncwarp();
-        int nt = warp0_exclusive_scan(sm.scratch, ws.tile_off, E, lane);
         if (lane == 0) {
-            ws.tile_off[E] = nt;
+            sm.off[E] = total;
             ws.ctrl->n_uniq = nu;
-            ws.ctrl->n_tiles_gu = nt;
         }
     }
     __syncthreads();
     for (int e = tid; e < E; e += nth) {
         ws.counts[e] = sm.cnt[e];
         ws.offsets[e] = sm.off[e];
-        sm.run[e] = 0;
+        ws.tile_off[e] = 0;  // the grouped GEMM tiles are unused on the small path
     }
-    if (tid == 0) ws.offsets[E] = sm.off[E];
-    const int chunk = sm.words * 32;
-    for (int base = 0; base < T; base += chunk) {
-        const int nt = min(chunk, T - base);
-        for (int i = tid; i < E * sm.words; i += nth) sm.bm[i] = 0u;
-        __syncthreads();
-        for (int i = tid; i < nt * k; i += nth) {
-            int t = base + i / k;
-            int e = ids[(size_t)t * k + (i % k)];
-            if ((unsigned)e < (unsigned)E) {
-                int tl = t - base;
-                atomicOr(&sm.bm[e * sm.words + (tl >> 5)], 1u << (tl & 31));
-            }
-        }
-        __syncthreads();
-        for (int e = warp; e < E; e += nwarps) {
-            int run = sm.run[e];
-            const int row0 = sm.off[e];
-            for (int wb = 0; wb < sm.words; wb += 32) {
-                int wi = wb + lane;
-                uint32_t word = wi < sm.words ? sm.bm[e * sm.words + wi] : 0u;
-                int c = __popc(word);
-                int incl = c;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-                    if (lane >= o) incl += y;
-                }
-                int r = run + incl - c;
-                while (word) {
-                    int b = __ffs(word) - 1;
-                    word &= word - 1;
-                    int t = base + wi * 32 + b;
-                    int row = row0 + r;
-                    ws.perm[row] = t;
-                    for (int j = 0; j < k; ++j)
-                        if (ids[(size_t)t * k + j] == e) ws.pos[(size_t)t * k + j] = row;
-                    ++r;
-                }
-                run += __shfl_sync(0xFFFFFFFFu, incl, 31);
-            }
-            if (lane == 0) sm.run[e] = run;
-        }
-        __syncthreads();
+    if (tid == 0) {
+        ws.offsets[E] = sm.off[E];
+        ws.tile_off[E] = 0;
+    }
+    for (int p = tid; p < Tk; p += nth) {
+        const int e = ids[p];
+        if ((unsigned)e >= (unsigned)E) continue;
+        const int t = p / k;
+        const int row = sm.off[e] + __popc(sm.bm[e] & ((1u << t) - 1u));
+        ws.perm[row] = t;
+        ws.pos[p] = row;
     }
 }
 
@@ -209,11 +175,14 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(const u
     const int eps = warp >> 2, q = warp & 3;
     const int e = blockIdx.x * kRouteExpertsPerCta + eps;
     const int nvec_q = d / 32;  // 16-byte vectors per quarter row
+    // the expert stage that follows is launched as a programmatic dependent
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     float acc[TM];
 #pragma unroll
     for (int t = 0; t < TM; ++t) acc[t] = 0.f;
     if (e < E) {
         const uint4 *wrow = reinterpret_cast<const uint4 *>(wr + (size_t)e * d) + q * nvec_q;
+#pragma unroll 4
         for (int v = lane; v < nvec_q; v += 32) {
             uint4 wv = __ldg(wrow + v);
             float wf[8] = {bf16lo(wv.x), bf16hi(wv.x), bf16lo(wv.y), bf16hi(wv.y),
@@ -264,7 +233,7 @@ __global__ void __launch_bounds__(kRouteSmallThreads) route_small_kernel(const u
     int32_t *si = reinterpret_cast<int32_t *>(smem_raw);
     PermSmem sm{si, si + (E + 1), si + 2 * (E + 1), si + 3 * (E + 1),
                 reinterpret_cast<uint32_t *>(si + 4 * (E + 1)), 1};
-    permute_block(ws.ids, T, k, E, ws, sm);
+    permute_block_small(ws.ids, T, k, E, ws, sm);
 }
 
 static size_t perm_smem_bytes(int E, int words) { return (size_t)4 * (E + 1) * 4 + (size_t)E * words * 4; }
@@ -293,37 +262,120 @@ cudaError_t launch_route_small(const LayerDev &L, const Workspace &ws, const uin
 }
 
 // ---------------------------------------------------------------------------
-// Large-T route: router GEMM on the tensor cores (prefill.cu), a top-k kernel
-// (one warp per token) and a one-CTA permutation kernel.
+// Large-T route: router GEMM on the tensor cores (prefill.cu), then
+//   route_chunk_kernel: one CTA per 256-token chunk runs top-k (one warp per
+//     token), builds the chunk's per-expert token bitmap and counts; the last
+//     CTA to finish scans the counts over experts and chunks;
+//   route_scatter_kernel: one CTA per chunk places every (token, slot) pair at
+//     chunk_base[chunk][e] + (tokens of e earlier in the chunk).
 // ---------------------------------------------------------------------------
-__global__ void topk_kernel(const float *__restrict__ logits, int T, int E, int k, int32_t *ids, float *w) {
-    int t = blockIdx.x * (blockDim.x / 32) + (threadIdx.x >> 5);
-    if (t >= T) return;
-    topk_warp(logits + (size_t)t * E, E, k, ids + (size_t)t * k, w + (size_t)t * k, false);
+constexpr int kChunk = 256;              // tokens per chunk
+constexpr int kChunkWords = kChunk / 32;
+
+__global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, Workspace ws) {
+    __shared__ uint32_t bm[256 * kChunkWords];
+    __shared__ int32_t s_cnt[257], s_off[257], s_flag[257], s_idx[257];
+    __shared__ int s_last;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int c = blockIdx.x, t0 = c * kChunk;
+    const int nt = min(kChunk, T - t0);
+    for (int i = tid; i < E * kChunkWords; i += 256) bm[i] = 0u;
+    __syncthreads();
+    for (int tl = warp; tl < nt; tl += 8) {
+        const int t = t0 + tl;
+        topk_warp(ws.logits + (size_t)t * E, E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false);
+        __syncwarp();
+        if (lane < k) {
+            const int e = ws.ids[(size_t)t * k + lane];
+            atomicOr(&bm[e * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+        }
+    }
+    __syncthreads();
+    uint32_t *gbm = ws.chunk_bm + (size_t)c * E * kChunkWords;
+    for (int i = tid; i < E * kChunkWords; i += 256) gbm[i] = bm[i];
+    for (int e = tid; e < E; e += 256) {
+        int n = 0;
+#pragma unroll
+        for (int w8 = 0; w8 < kChunkWords; ++w8) n += __popc(bm[e * kChunkWords + w8]);
+        ws.chunk_base[(size_t)c * E + e] = n;
+    }
+    // last-CTA hand-off: the CTA that completes the count scans for everyone
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) s_last = (atomicAdd(&ws.ctrl->route_done, 1u) == gridDim.x - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    const int nch = gridDim.x;
+    for (int e = tid; e < E; e += 256) {
+        int n = 0;
+        for (int cc = 0; cc < nch; ++cc) n += __ldcg(ws.chunk_base + (size_t)cc * E + e);
+        s_cnt[e] = n;
+        s_flag[e] = n > 0 ? 1 : 0;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int total = warp0_exclusive_scan(s_cnt, s_off, E, lane);
+        const int nu = warp0_exclusive_scan(s_flag, s_idx, E, lane);
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) {
+            if (s_cnt[e] > 0) ws.uniq[s_idx[e]] = e;
+            s_flag[e] = (s_cnt[e] + 127) >> 7;       // 128-row tiles of the grouped GEMMs
+        }
+        __syncwarp();
+        const int ntile = warp0_exclusive_scan(s_flag, ws.tile_off, E, lane);
+        if (lane == 0) {
+            s_off[E] = total;
+            ws.offsets[E] = total;
+            ws.tile_off[E] = ntile;
+            ws.ctrl->n_uniq = nu;
+            ws.ctrl->n_tiles_gu = ntile;
+            ws.ctrl->route_done = 0u;
+        }
+    }
+    __syncthreads();
+    for (int e = tid; e < E; e += 256) {
+        ws.counts[e] = s_cnt[e];
+        ws.offsets[e] = s_off[e];
+        int run = s_off[e];
+        for (int cc = 0; cc < nch; ++cc) {   // chunk counts -> first row of each chunk
+            const size_t i = (size_t)cc * E + e;
+            const int n = __ldcg(ws.chunk_base + i);
+            ws.chunk_base[i] = run;
+            run += n;
+        }
+    }
 }
 
-constexpr int kPermWords = 64;  // 2048 tokens per bitmap chunk
-
-__global__ void __launch_bounds__(1024) permute_kernel(int T, int k, int E, Workspace ws) {
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    int32_t *si = reinterpret_cast<int32_t *>(smem_raw);
-    PermSmem sm{si, si + (E + 1), si + 2 * (E + 1), si + 3 * (E + 1),
-                reinterpret_cast<uint32_t *>(si + 4 * (E + 1)), kPermWords};
-    permute_block(ws.ids, T, k, E, ws, sm);
+__global__ void __launch_bounds__(256) route_scatter_kernel(int T, int k, int E, Workspace ws) {
+    const int c = blockIdx.x, t0 = c * kChunk;
+    const int nt = min(kChunk, T - t0);
+    const uint32_t *gbm = ws.chunk_bm + (size_t)c * E * kChunkWords;
+    for (int p = threadIdx.x; p < nt * k; p += 256) {
+        const int tl = p / k;
+        const int t = t0 + tl;
+        const int e = ws.ids[(size_t)t0 * k + p];
+        if ((unsigned)e >= (unsigned)E) {
+            atomicOr(&ws.ctrl->err, ERRBIT_RANGE);
+            continue;
+        }
+        const uint32_t *b = gbm + e * kChunkWords;
+        int rank = 0;
+        for (int w8 = 0; w8 < (tl >> 5); ++w8) rank += __popc(b[w8]);
+        rank += __popc(b[tl >> 5] & ((1u << (tl & 31)) - 1u));
+        const int row = ws.chunk_base[(size_t)c * E + e] + rank;
+        ws.perm[row] = t;
+        ws.pos[(size_t)t0 * k + p] = row;
+    }
 }
 
 cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
                                int *launches) {
     cudaError_t e = launch_router_gemm(L, ws, x, T, st);
     if (e != cudaSuccess) return e;
-    topk_kernel<<<(T + 7) / 8, 256, 0, st>>>(ws.logits, T, L.E, L.k, ws.ids, ws.w);
-    size_t smem = perm_smem_bytes(L.E, kPermWords);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaFuncSetAttribute(permute_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        attr_set = true;
-    }
-    permute_kernel<<<1, 1024, smem, st>>>(T, L.k, L.E, ws);
+    const int nch = (T + kChunk - 1) / kChunk;
+    route_chunk_kernel<<<nch, 256, 0, st>>>(T, L.k, L.E, ws);
+    route_scatter_kernel<<<nch, 256, 0, st>>>(T, L.k, L.E, ws);
     *launches += 3;
     return cudaGetLastError();
 }

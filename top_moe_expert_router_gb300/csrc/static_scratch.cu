@@ -93,16 +93,14 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
     L.gu = desc->g_up;
     L.gd = desc->g_down;
     L.num_sms = g_num_sms[dev];
+    L.expert_norm = desc->expert_out_norm ? 1 : 0;
     const Workspace ws = workspace_layout(g_scratch_ptr[dev], L.d, L.E, L.k, L.I, T);
 
     cudaStream_t st = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the control words (error
     // bits, the router's arrival counter) must start at zero
     if (cudaMemsetAsync(ws.ctrl, 0, sizeof(Control), st) != cudaSuccess) return MOE_ERR_CUDA;
-    const uint16_t *xs = (const uint16_t *)x;
-    cudaError_t e = launch_route_small(L, ws, xs, T, st);
-    if (e == cudaSuccess) e = launch_decode_gateup(L, ws, xs, T, st);
-    if (e == cudaSuccess) e = launch_decode_down(L, ws, xs, T, st);
-    if (e == cudaSuccess) e = launch_combine(L, ws, nullptr, (uint16_t *)out, T, st);
+    // the same single-launch layer kernel moe_forward runs for T <= 16
+    const cudaError_t e = launch_decode_fused(L, ws, (const uint16_t *)x, nullptr, (uint16_t *)out, T, st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
