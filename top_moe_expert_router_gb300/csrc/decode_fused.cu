@@ -52,7 +52,7 @@ struct Args {
     const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
     const float *gg, *gu, *gd;
     int T, d, I, E, k;
-    int nslots, ncons;
+    int nslots, ncons, nprod;
     uint32_t slot_bytes;
     int x_in_smem;            // tokens' rows staged in shared memory
     int do_combine;           // 0: leave Y for a separate combine kernel
@@ -111,7 +111,6 @@ __device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, vola
                 ok = 0;
                 break;
             }
-            __nanosleep(64);
         }
         __threadfence();
     }
@@ -238,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     int *cb_rows_s = reinterpret_cast<int *>(smem + 528);   // [32]
     int *cb_todo = cb_rows_s + 32;                  // [32]
     int *n_todo = cb_todo + 32;
+    float *xscale = reinterpret_cast<float *>(smem + 800);  // [16] NVFP4: per-token max|x|
     float *part = reinterpret_cast<float *>(smem + 1024);   // [8 warps][TM] router partials
     unsigned char *rbase = smem + 2048;             // routing scratch (8 KB)
     Route R;
@@ -274,21 +274,34 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     // ---- 1. router: logits of this CTA's experts ----
     // experts b, b + G, b + 2G, ... two at a time: warps 0-3 / 4-7 take the
     // four quarters of one expert's row
-    if (x_bytes && !mbar_wait_or_abort(xbar, 0, err, abort_flag)) {
-        // fall through: the grid barrier below reports and unwinds
-    }
     {
-        const int nq = d / 32;  // 16-byte vectors per quarter row
+        const int nq = d / 32;  // 16-byte vectors per quarter row (<= 256: at most 8 per lane)
+        bool x_ready = x_bytes == 0;
         for (int base = b; base < E; base += 2 * G) {
             const int eidx = base + (warp >= 4 ? G : 0);
             const int q = warp & 3;
             float acc[TM];
 #pragma unroll
             for (int t = 0; t < TM; ++t) acc[t] = 0.f;
-            if (warp < 8 && eidx < E) {
-                const uint4 *wrow = reinterpret_cast<const uint4 *>(a.wr + (size_t)eidx * d) + q * nq;
-                for (int v = lane; v < nq; v += 32) {
-                    const uint4 wv = __ldg(wrow + v);
+            // the router rows are requested before waiting for the tokens' copy
+            uint4 wpre[8];
+            const bool mine = warp < 8 && eidx < E;
+            const uint4 *wrow = reinterpret_cast<const uint4 *>(a.wr + (size_t)eidx * d) + q * nq;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int v = lane + 32 * j;
+                wpre[j] = (mine && v < nq) ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
+            }
+            if (!x_ready) {
+                mbar_wait_or_abort(xbar, 0, err, abort_flag);  // a timeout unwinds at the grid barrier below
+                x_ready = true;
+            }
+            if (mine) {
+#pragma unroll
+                for (int j = 0; j < 8; ++j) {
+                    const int v = lane + 32 * j;
+                    if (v >= nq) continue;
+                    const uint4 wv = wpre[j];
 #pragma unroll
                     for (int t = 0; t < TM; ++t) {
                         if (t < T) {
@@ -323,8 +336,33 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             }
             __syncthreads();
         }
+        if (!x_ready) mbar_wait_or_abort(xbar, 0, err, abort_flag);  // CTAs without router rows
     }
     grid_barrier(&ctrl->grid_bar, (uint32_t)G, err, abort_flag);
+
+    if (FP4 && x_bytes) {
+        // NVFP4 gate/up sums in fp16: keep the staged tokens as fp16(x / max|x|)
+        for (int t = warp; t < T; t += kConsumers + 1) {
+            const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs + (size_t)t * d * 2);
+            float m = 0.f;
+            for (int i = lane; i < d / 2; i += 32) {
+                const uint32_t wv = xw[i];
+                m = fmaxf(m, fmaxf(fabsf(bf16lo(wv)), fabsf(bf16hi(wv))));
+            }
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+            if (lane == 0) xscale[t] = m > 0.f ? m : 1.f;
+        }
+        __syncthreads();
+        for (int i = tid; i < T * (d / 2); i += kThreads) {
+            const float inv = 1.f / xscale[i / (d / 2)];
+            uint32_t *xw = reinterpret_cast<uint32_t *>(xs) + i;
+            const uint32_t wv = *xw;
+            const __half2 hv = __floats2half2_rn(bf16lo(wv) * inv, bf16hi(wv) * inv);
+            *xw = *reinterpret_cast<const uint32_t *>(&hv);
+        }
+        __syncthreads();
+    }
 
     // ---- 2. routing, computed by every CTA in shared memory ----
     for (int t = warp; t < T; t += kConsumers + 1)
@@ -395,10 +433,15 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     const uint32_t rbg = rowb<FP4>(d), rbd = rowb<FP4>(I);
 
     if (warp == kProducerWarp) {
-        if (lane == 0 && !*abort_flag) {
+        // a.nprod lanes fill the ring, lane l the slots j with j % nprod == l
+        // (nslots is a multiple of nprod), so every slot's fills come from one
+        // lane in order and the per-fill latency of a single issuing thread
+        // is overlapped nprod ways
+        const int P = a.nprod;
+        if (lane < P && !*abort_flag) {
             const uint64_t pol = policy_evict_first();
-            int s = 0;
-            for (; s < n_st; ++s) {
+            int s = lane;
+            for (; s < n_st; s += P) {
                 const int slot = s % NS;
                 if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
                 unsigned char *dst = ring + (size_t)slot * a.slot_bytes;
@@ -431,8 +474,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                     }
                 }
             }
-            // every copy issued must land before the CTA moves on
-            for (int j = (s > NS ? s - NS : 0); j < s; ++j) mbar_wait(&full[j % NS], (j / NS) & 1, err);
+            // every copy this lane issued must land before the CTA moves on
+            for (int j = lane; j < s; j += P)
+                if (j + NS >= s) mbar_wait(&full[j % NS], (j / NS) & 1, err);
         }
     } else if (warp < C) {
         // ------------------------------- gate/up -------------------------------
@@ -449,33 +493,114 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
 #pragma unroll
             for (int r = 0; r < TM; ++r) ag[r] = au[r] = make_float2(0.f, 0.f);
             if (!FP4) {
+                constexpr int kXV = 8;
                 const uint4 *gw = reinterpret_cast<const uint4 *>(st);
                 const uint4 *uw = reinterpret_cast<const uint4 *>(st + rbg);
+                const int nvec = d / 8;
+                if (a.x_in_smem) {
+                    // vector by vector: each weight vector is unpacked once and
+                    // used for every token of the expert
 #pragma unroll 2
-                for (int v = lane; v < d / 8; v += 32) {
-                    const uint4 g4 = gw[v], u4 = uw[v];
-                    const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
-                    const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
+                    for (int v = lane; v < nvec; v += 32) {
+                        const uint4 g4 = gw[v], u4 = uw[v];
+                        const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
+                        const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < seg.n_e) {
-                            const uint4 xv =
-                                a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v]
-                                            : __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + v);
-                            const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
-                            ag[r] = ffma2(g0, x0, ag[r]);
-                            au[r] = ffma2(u0, x0, au[r]);
-                            ag[r] = ffma2(g1, x1, ag[r]);
-                            au[r] = ffma2(u1, x1, au[r]);
-                            ag[r] = ffma2(g2, x2, ag[r]);
-                            au[r] = ffma2(u2, x2, au[r]);
-                            ag[r] = ffma2(g3, x3, ag[r]);
-                            au[r] = ffma2(u3, x3, au[r]);
+                        for (int r = 0; r < TM; ++r) {
+                            if (r < seg.n_e) {
+                                const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v];
+                                const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
+                                ag[r] = ffma2(g0, x0, ag[r]);
+                                au[r] = ffma2(u0, x0, au[r]);
+                                ag[r] = ffma2(g1, x1, ag[r]);
+                                au[r] = ffma2(u1, x1, au[r]);
+                                ag[r] = ffma2(g2, x2, ag[r]);
+                                au[r] = ffma2(u2, x2, au[r]);
+                                ag[r] = ffma2(g3, x3, ag[r]);
+                                au[r] = ffma2(u3, x3, au[r]);
+                            }
+                        }
+                    }
+                } else {
+                // token by token; each lane's vectors in chunks of kXV whose
+                // token loads (from global memory) are all issued before the
+                // arithmetic: one latency per chunk
+#pragma unroll
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const uint4 *xrow = a.x_in_smem
+                                                ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)
+                                                : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d);
+                        for (int j0 = 0; j0 * 32 < nvec; j0 += kXV) {
+                            uint4 xv[kXV];
+#pragma unroll
+                            for (int jj = 0; jj < kXV; ++jj) {
+                                const int v = lane + 32 * (j0 + jj);
+                                xv[jj] = v < nvec ? (a.x_in_smem ? xrow[v] : __ldg(xrow + v)) : make_uint4(0, 0, 0, 0);
+                            }
+#pragma unroll
+                            for (int jj = 0; jj < kXV; ++jj) {
+                                const int v = lane + 32 * (j0 + jj);
+                                if (v < nvec) {
+                                    const uint4 g4 = gw[v], u4 = uw[v];
+                                    const float2 x0 = bf2(xv[jj].x), x1 = bf2(xv[jj].y), x2 = bf2(xv[jj].z),
+                                                 x3 = bf2(xv[jj].w);
+                                    ag[r] = ffma2(bf2(g4.x), x0, ag[r]);
+                                    au[r] = ffma2(bf2(u4.x), x0, au[r]);
+                                    ag[r] = ffma2(bf2(g4.y), x1, ag[r]);
+                                    au[r] = ffma2(bf2(u4.y), x1, au[r]);
+                                    ag[r] = ffma2(bf2(g4.z), x2, ag[r]);
+                                    au[r] = ffma2(bf2(u4.z), x2, au[r]);
+                                    ag[r] = ffma2(bf2(g4.w), x3, ag[r]);
+                                    au[r] = ffma2(bf2(u4.w), x3, au[r]);
+                                }
+                            }
                         }
                     }
                 }
+                }
             } else {
                 const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rbg, *us = st + rbg + d / 2;
+                if (a.x_in_smem) {
+                    // tokens in shared memory as fp16(x / max|x|): the 16 products
+                    // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
+                    // pairs, then scaled by the block scale and max|x| in fp32
+                    for (int bb = lane; bb < d / 16; bb += 32) {
+                        const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
+                        const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
+                        __half2 gh[8], uh[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t gw_ = q < 4 ? gqv.x : gqv.y, uw_ = q < 4 ? uqv.x : uqv.y;
+                            __half2_raw g2 = __nv_cvt_fp4x2_to_halfraw2(
+                                (__nv_fp4x2_storage_t)((gw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
+                            __half2_raw u2 = __nv_cvt_fp4x2_to_halfraw2(
+                                (__nv_fp4x2_storage_t)((uw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
+                            gh[q] = *reinterpret_cast<__half2 *>(&g2);
+                            uh[q] = *reinterpret_cast<__half2 *>(&u2);
+                        }
+                        const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
+#pragma unroll
+                        for (int r = 0; r < TM; ++r) {
+                            if (r < seg.n_e) {
+                                const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2;
+                                const uint4 xa = xp[0], xb = xp[1];
+                                const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                                __half2 pg = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+                                __half2 pu = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+#pragma unroll
+                                for (int q = 1; q < 8; ++q) {
+                                    pg = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg);
+                                    pu = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu);
+                                }
+                                const float2 fg = __half22float2(pg), fu = __half22float2(pu);
+                                const float xsc = xscale[seg.tok[r]];
+                                ag[r].x = fmaf(fg.x + fg.y, sgb * xsc, ag[r].x);
+                                au[r].x = fmaf(fu.x + fu.y, sub * xsc, au[r].x);
+                            }
+                        }
+                    }
+                } else
                 for (int bb = lane; bb < d / 16; bb += 32) {
                     float2 gf[8], uf[8];
                     fp4x16(*reinterpret_cast<const uint2 *>(gq + bb * 8), gf);
@@ -528,13 +653,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                     *abort_flag = 1;
                     break;
                 }
-                __nanosleep(64);
-            }
+                }
             __threadfence();
         }
         named_bar(1, 32 * C);
         // ---------------------------------- down ----------------------------------
         Seg<TM> sd;
+        // an expert with one token: its h row stays in registers for all the
+        // warp's stages of that expert (I <= 2048)
+        constexpr int kHC = TM <= 2 ? 8 : 1;
+        float4 hc0[kHC], hc1[kHC];
+        int hc_u = -1;
         for (; s < n_st && !*abort_flag; s += C) {
             const int slot = s % NS;
             const int g = (dn_b + (s - n_gu)) * kDnRows;
@@ -549,23 +678,70 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
 #pragma unroll
                 for (int r = 0; r < TM; ++r) acc[q][r] = make_float2(0.f, 0.f);
             if (!FP4) {
-                for (int v = lane; v < I / 8; v += 32) {
-                    uint4 wv[kDnRows];
+                // token by token; h (in L2, written by other CTAs) fetched in
+                // chunks of kHV vectors per lane, all loads of a chunk issued
+                // before its arithmetic
+                constexpr int kHV = TM >= 8 ? 4 : 8;
+                const int nvec = I / 8;
+                if (TM <= 2 && sd.n_e == 1 && nvec <= 32 * kHC) {
+                    if (hc_u != sd.u) {
+                        const float4 *hr = reinterpret_cast<const float4 *>(hrow);
 #pragma unroll
-                    for (int q = 0; q < kDnRows; ++q) wv[q] = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                        for (int jj = 0; jj < kHC; ++jj) {
+                            const int v = lane + 32 * jj;
+                            if (v < nvec) {
+                                hc0[jj] = __ldcg(hr + 2 * v);
+                                hc1[jj] = __ldcg(hr + 2 * v + 1);
+                            }
+                        }
+                        hc_u = sd.u;
+                    }
 #pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < sd.n_e) {
-                            const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + v * 8);
-                            const float4 h0 = __ldcg(hp), h1 = __ldcg(hp + 1);
-                            const float2 ha = make_float2(h0.x, h0.y), hb = make_float2(h0.z, h0.w);
-                            const float2 hc = make_float2(h1.x, h1.y), hd = make_float2(h1.z, h1.w);
+                    for (int jj = 0; jj < kHC; ++jj) {
+                        const int v = lane + 32 * jj;
+                        if (v < nvec) {
+                            const float2 ha = make_float2(hc0[jj].x, hc0[jj].y), hb = make_float2(hc0[jj].z, hc0[jj].w);
+                            const float2 hc = make_float2(hc1[jj].x, hc1[jj].y), hd = make_float2(hc1[jj].z, hc1[jj].w);
 #pragma unroll
                             for (int q = 0; q < kDnRows; ++q) {
-                                acc[q][r] = ffma2(bf2(wv[q].x), ha, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv[q].y), hb, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv[q].z), hc, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv[q].w), hd, acc[q][r]);
+                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                                acc[q][0] = ffma2(bf2(wv.x), ha, acc[q][0]);
+                                acc[q][0] = ffma2(bf2(wv.y), hb, acc[q][0]);
+                                acc[q][0] = ffma2(bf2(wv.z), hc, acc[q][0]);
+                                acc[q][0] = ffma2(bf2(wv.w), hd, acc[q][0]);
+                            }
+                        }
+                    }
+                } else
+#pragma unroll
+                for (int r = 0; r < TM; ++r) {
+                    if (r < sd.n_e) {
+                        const float4 *hr = reinterpret_cast<const float4 *>(hrow + (size_t)r * I);
+                        for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
+                            float4 h0[kHV], h1[kHV];
+#pragma unroll
+                            for (int jj = 0; jj < kHV; ++jj) {
+                                const int v = lane + 32 * (j0 + jj);
+                                if (v < nvec) {
+                                    h0[jj] = __ldcg(hr + 2 * v);
+                                    h1[jj] = __ldcg(hr + 2 * v + 1);
+                                }
+                            }
+#pragma unroll
+                            for (int jj = 0; jj < kHV; ++jj) {
+                                const int v = lane + 32 * (j0 + jj);
+                                if (v < nvec) {
+                                    const float2 ha = make_float2(h0[jj].x, h0[jj].y), hb = make_float2(h0[jj].z, h0[jj].w);
+                                    const float2 hc = make_float2(h1[jj].x, h1[jj].y), hd = make_float2(h1[jj].z, h1[jj].w);
+#pragma unroll
+                                    for (int q = 0; q < kDnRows; ++q) {
+                                        const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                                        acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
+                                        acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
+                                        acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
+                                        acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
+                                    }
+                                }
                             }
                         }
                     }
@@ -729,6 +905,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     if (fixed + xb2 + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
     const int fit = (int)((kSmemBudget - fixed - xb2) / a.slot_bytes);
     a.nslots = pick<FP4>(fit, a.ncons);
+    a.nprod = a.nslots % 4 == 0 ? 4 : (a.nslots % 2 == 0 ? 2 : 1);
     const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
     static bool attr = false;
     if (!attr) {
