@@ -30,7 +30,8 @@ struct Control {
     int32_t n_tiles_dn;      // prefill: down tiles
     uint32_t grid_bar;       // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
     uint32_t grid_exit;      // fused decode kernel: CTAs that finished
-    uint32_t pad[26];
+    uint32_t h_ready[2];     // fused decode kernel: h rows written, first / second half of the experts
+    uint32_t pad[24];
     uint32_t cb_rows[32];    // fused decode kernel: expert rows done per 256-column block of Y
 };
 

@@ -16,9 +16,11 @@
 //      copies: first this CTA's share of the active experts' gate/up rows,
 //      then, without a pause, its share of their down rows; slot j belongs
 //      to consumer warp j % c, which takes the slot's phases in order;
-//   4. consumer warps compute h = silu(Wg x) * (Wu x) (fp32, to global), meet
-//      at a grid barrier (all of h written) while the producer keeps
-//      fetching down rows, then compute Y = Wd h (fp32, to global);
+//   4. consumer warps compute h = silu(Wg x) * (Wu x) (fp32, to global) and
+//      count the rows in, per half of the active experts; the stream runs
+//      first-half gate/up, second-half gate/up, first-half down, second-half
+//      down, so a half's h is complete long before its down rows arrive and
+//      the weight stream never pauses; then Y = Wd h (fp32, to global);
 //   5. combine: per 256-column block of the output, the CTA whose down rows
 //      complete the block (a row counter per block) forms
 //      out = (res +) sum_j w_j Y_j for those columns, in fp32, j ascending.
@@ -116,6 +118,60 @@ __device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, vola
     }
     __syncthreads();
     return ok != 0;
+}
+
+// This CTA's stages: segment A = first-half gate/up row pairs, B = second-half
+// gate/up, C = first-half down units (kDnRows rows), D = second-half down.
+struct Plan {
+    int nA, nB, nC, nD;        // stages of each segment in this CTA
+    int a0, b0, c0, d0;        // first index of this CTA's share within each segment
+    int offB, offD;            // global start of the second-half segments
+    // flattened gate/up row-pair index (u * I + i) of gate/up stage s
+    __device__ __forceinline__ int gu_row(int s) const { return s < nA ? a0 + s : offB + b0 + (s - nA); }
+    // flattened down unit index (u * d / kDnRows + c / kDnRows) of down stage t (t = s - nA - nB)
+    __device__ __forceinline__ int dn_unit(int t) const { return t < nC ? c0 + t : offD + d0 + (t - nC); }
+};
+
+__device__ __forceinline__ void share(int total, int b, int G, int &start, int &count) {
+    start = (int)((long long)b * total / G);
+    count = (int)((long long)(b + 1) * total / G) - start;
+}
+
+__device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, int b, int G) {
+    Plan p;
+    const int U1 = (U + 1) / 2, U2 = U - U1;
+    share(U1 * I, b, G, p.a0, p.nA);
+    share(U2 * I, b, G, p.b0, p.nB);
+    share(U1 * units_per_expert, b, G, p.c0, p.nC);
+    share(U2 * units_per_expert, b, G, p.d0, p.nD);
+    p.offB = U1 * I;
+    p.offD = U1 * units_per_expert;
+    return p;
+}
+
+// Publish a warp's count of finished h rows (all lanes' h stores first).
+__device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
+    __threadfence();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0 && n) atomicAdd(ctr, (uint32_t)n);
+}
+
+// Warp-wide bounded wait until *ctr >= target.
+__device__ __forceinline__ bool wait_rows(const uint32_t *ctr, uint32_t target, uint32_t *err,
+                                          volatile int *abort_flag) {
+    int ok = 1;
+    if ((threadIdx.x & 31) == 0) {
+        const unsigned long long t0 = global_ns();
+        while (ld_acquire(ctr) < target) {
+            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
+                atomicOr(err, ERRBIT_TIMEOUT);
+                *abort_flag = 1;
+                ok = 0;
+                break;
+            }
+        }
+    }
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 // Per-warp cache of the expert a stage belongs to (read from shared memory).
@@ -423,13 +479,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     }
 
     // ---- 3./4. the weight stream ----
-    const int gu_total = n_uniq * I;
-    const int gu_b = (int)((long long)b * gu_total / G);
-    const int n_gu = (int)((long long)(b + 1) * gu_total / G) - gu_b;
-    const int dn_total = n_uniq * (d / kDnRows);
-    const int dn_b = (int)((long long)b * dn_total / G);
-    const int n_dn = (int)((long long)(b + 1) * dn_total / G) - dn_b;
-    const int n_st = n_gu + n_dn;
+    // The active experts are split in two halves, H1 = the first ceil(U/2).
+    // Every CTA streams its share of, in order: H1 gate/up rows, H2 gate/up
+    // rows, H1 down rows, H2 down rows. Down rows of a half wait for that
+    // half's h (a global row count), which the other CTAs finished a whole
+    // segment earlier, so the stream does not stop between the two
+    // projections. A wait only ever sits at a down stage, and every stage that
+    // feeds the counts comes earlier in every CTA's order, so the waits end.
+    const Plan pl = make_plan(n_uniq, I, d / kDnRows, b, G);
+    const int n_gu = pl.nA + pl.nB;
+    const int n_st = n_gu + pl.nC + pl.nD;
+    const int U1 = (n_uniq + 1) / 2;
     const uint32_t rbg = rowb<FP4>(d), rbd = rowb<FP4>(I);
 
     if (warp == kProducerWarp) {
@@ -446,7 +506,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                 if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
                 unsigned char *dst = ring + (size_t)slot * a.slot_bytes;
                 if (s < n_gu) {
-                    const int g = gu_b + s;
+                    const int g = pl.gu_row(s);
                     const int u = g / I, i = g - u * I;
                     const size_t row = (size_t)R.uniq[u] * I + i;
                     mbar_arrive_expect_tx(&full[slot], 2 * rbg);
@@ -461,7 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                         bulk_g2s(dst + rbg + nq, a.su + row * nsb, nsb, &full[slot], pol);
                     }
                 } else {
-                    const int g = (dn_b + (s - n_gu)) * kDnRows;
+                    const int g = pl.dn_unit(s - n_gu) * kDnRows;
                     const int u = g / d, c0 = g - u * d;
                     const size_t row = (size_t)R.uniq[u] * d + c0;
                     mbar_arrive_expect_tx(&full[slot], kDnRows * rbd);
@@ -482,9 +542,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
         // ------------------------------- gate/up -------------------------------
         Seg<TM> seg;
         int s = warp;
+        int done_a = 0, done_b = 0;   // this warp's finished h rows of each half
+        bool pub_a = false;
         for (; s < n_gu && !*abort_flag; s += C) {
+            if (s >= pl.nA && !pub_a) {
+                publish_rows(&ctrl->h_ready[0], done_a);
+                pub_a = true;
+            }
+            if (s < pl.nA)
+                ++done_a;
+            else
+                ++done_b;
             const int slot = s % NS;
-            const int g = gu_b + s;
+            const int g = pl.gu_row(s);
             const int u = g / I, i = g - u * I;
             if (u != seg.u) seg_load(seg, R, u);
             if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
@@ -630,33 +700,35 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
-            float hv = 0.f;
+            if (seg.n_e == 1) {
+                // one token: lanes < 16 reduce the gate sum, lanes >= 16 the up sum
+                const bool hi = lane & 16;
+                const float gs_ = ag[0].x + ag[0].y, us_ = au[0].x + au[0].y;
+                float kk = hi ? us_ : gs_;
+                kk += __shfl_xor_sync(0xFFFFFFFFu, hi ? gs_ : us_, 16);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 8);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
+                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
+                const float up_total = __shfl_sync(0xFFFFFFFFu, kk, 16);
+                if (lane == 0) a.ws.h[(size_t)seg.row0 * I + i] = silu(kk * gsc) * (up_total * usc);
+            } else {
+                float hv = 0.f;
 #pragma unroll
-            for (int r = 0; r < TM; ++r) {
-                if (r < seg.n_e) {
-                    const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
-                    const float su_ = warp_sum(au[r].x + au[r].y) * usc;
-                    if (lane == r) hv = silu(sg_) * su_;
+                for (int r = 0; r < TM; ++r) {
+                    if (r < seg.n_e) {
+                        const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
+                        const float su_ = warp_sum(au[r].x + au[r].y) * usc;
+                        if (lane == r) hv = silu(sg_) * su_;
+                    }
                 }
+                if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
             }
-            if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
         }
-        // all consumer warps of every CTA have written their h: grid barrier
-        named_bar(1, 32 * C);
-        if (warp == 0 && lane == 0) {
-            __threadfence();
-            atomicAdd(&ctrl->grid_bar, 1u);
-            const unsigned long long t0 = global_ns();
-            while (ld_acquire(&ctrl->grid_bar) < 2u * G) {
-                if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                    atomicOr(err, ERRBIT_TIMEOUT);
-                    *abort_flag = 1;
-                    break;
-                }
-                }
-            __threadfence();
-        }
-        named_bar(1, 32 * C);
+        // this warp's h rows are written: count them in
+        if (!pub_a) publish_rows(&ctrl->h_ready[0], done_a);
+        publish_rows(&ctrl->h_ready[1], done_b);
+        bool ready_a = false, ready_b = false;
         // ---------------------------------- down ----------------------------------
         Seg<TM> sd;
         // an expert with one token: its h row stays in registers for all the
@@ -665,8 +737,17 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
         float4 hc0[kHC], hc1[kHC];
         int hc_u = -1;
         for (; s < n_st && !*abort_flag; s += C) {
+            const int t = s - n_gu;
+            if (t < pl.nC && !ready_a) {
+                if (!wait_rows(&ctrl->h_ready[0], (uint32_t)(U1 * I), err, abort_flag)) break;
+                ready_a = true;
+            }
+            if (t >= pl.nC && !ready_b) {
+                if (!wait_rows(&ctrl->h_ready[1], (uint32_t)((n_uniq - U1) * I), err, abort_flag)) break;
+                ready_b = true;
+            }
             const int slot = s % NS;
-            const int g = (dn_b + (s - n_gu)) * kDnRows;
+            const int g = pl.dn_unit(t) * kDnRows;
             const int u = g / d, c0 = g - u * d;
             if (u != sd.u) seg_load(sd, R, u);
             if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
@@ -774,17 +855,39 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
             const float gsc = FP4 ? a.gd[sd.e] : 1.f;
+            if (sd.n_e == 1) {
+                // one token: reduce the four rows' partial sums together,
+                // exchanging halves so that lane group q ends with row q
+                static_assert(kDnRows == 4, "the transposed reduction takes four rows");
+                float r0 = acc[0][0].x + acc[0][0].y, r1 = acc[1][0].x + acc[1][0].y;
+                float r2 = acc[2][0].x + acc[2][0].y, r3 = acc[3][0].x + acc[3][0].y;
+                const bool hi16 = lane & 16, hi8 = lane & 8;
+                // step 1: lanes < 16 keep rows 0,1; lanes >= 16 keep rows 2,3
+                float k0 = hi16 ? r2 : r0, k1 = hi16 ? r3 : r1;
+                const float s0 = hi16 ? r0 : r2, s1 = hi16 ? r1 : r3;
+                k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+                k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+                // step 2: within each half, lanes with bit 3 clear keep the first row
+                float k = hi8 ? k1 : k0;
+                k += __shfl_xor_sync(0xFFFFFFFFu, hi8 ? k0 : k1, 8);
+                k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
+                k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+                k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+                // lane groups of 8: [0,8) row 0, [8,16) row 1, [16,24) row 2, [24,32) row 3
+                if ((lane & 7) == 0) a.ws.Y[(size_t)sd.row0 * d + c0 + (lane >> 3)] = k * gsc;
+            } else {
 #pragma unroll
-            for (int q = 0; q < kDnRows; ++q) {
-                float yv = 0.f;
+                for (int q = 0; q < kDnRows; ++q) {
+                    float yv = 0.f;
 #pragma unroll
-                for (int r = 0; r < TM; ++r) {
-                    if (r < sd.n_e) {
-                        const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
-                        if (lane == r) yv = sum * gsc;
+                    for (int r = 0; r < TM; ++r) {
+                        if (r < sd.n_e) {
+                            const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
+                            if (lane == r) yv = sum * gsc;
+                        }
                     }
+                    if (lane < sd.n_e) a.ws.Y[(size_t)(sd.row0 + lane) * d + c0 + q] = yv;
                 }
-                if (lane < sd.n_e) a.ws.Y[(size_t)(sd.row0 + lane) * d + c0 + q] = yv;
             }
             if (lane == 0) atomicAdd(&cb_rows_s[c0 / kCb], kDnRows);
         }
@@ -846,6 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
         if (atomicAdd(&ctrl->grid_exit, 1u) == (uint32_t)G - 1) {
             for (int cb = 0; cb < 32; ++cb) ctrl->cb_rows[cb] = 0u;  // zero already unless a wait gave up
             ctrl->grid_bar = 0u;
+            ctrl->h_ready[0] = 0u;
+            ctrl->h_ready[1] = 0u;
             ctrl->grid_exit = 0u;
             __threadfence();
         }
