@@ -22,17 +22,24 @@ constexpr unsigned long long kWaitLimitNs = 1500000000ull;  // 1.5 s
 // Workspace layout. All regions 256-byte aligned; sizes depend on the layer
 // shape and max_tokens only.
 // ---------------------------------------------------------------------------
+// One counter alone on a 128-byte line: counters that many CTAs update or poll
+// at once do not share a line with each other.
+struct CtrLine {
+    uint32_t v;
+    uint32_t pad[31];
+};
+
 struct Control {
     uint32_t err;            // error bits
     uint32_t route_done;     // arrival counter of the router's CTAs (reset by the last)
     int32_t n_uniq;          // number of experts with at least one token
     int32_t n_tiles_gu;      // prefill: gate/up tiles
     int32_t n_tiles_dn;      // prefill: down tiles
-    uint32_t grid_bar;       // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
-    uint32_t grid_exit;      // fused decode kernel: CTAs that finished
-    uint32_t h_ready[2];     // fused decode kernel: h rows written, first / second half of the experts
-    uint32_t pad[24];
-    uint32_t cb_rows[32];    // fused decode kernel: expert rows done per 256-column block of Y
+    uint32_t pad0[27];
+    CtrLine grid_bar;        // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
+    CtrLine grid_exit;       // fused decode kernel: CTAs that finished
+    CtrLine h_ready[2];      // fused decode kernel: h rows written, first / second half of the experts
+    CtrLine cb_rows[32];     // fused decode kernel: expert rows done per 256-column block of Y
 };
 
 struct Workspace {
@@ -105,6 +112,12 @@ __device__ __forceinline__ unsigned long long global_ns() {
     return t;
 }
 
+// Release/acquire fence at GPU scope: with a relaxed atomic it orders this
+// thread's earlier stores before the atomic (release side), or the atomic's
+// observation before later loads (acquire side). Cheaper than the sequentially
+// consistent __threadfence(), whose total order these hand-offs do not need.
+__device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_rel.gpu;" ::: "memory"); }
+
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
@@ -129,6 +142,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
         "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Non-blocking test: has the phase of `bar` with the given parity completed?
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)

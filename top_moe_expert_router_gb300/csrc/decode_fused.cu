@@ -36,7 +36,7 @@ namespace moe {
 
 namespace fused {
 
-constexpr int kConsumers = 8;                 // consumer warps at most
+constexpr int kConsumers = 7;                 // consumer warps at most (8 warps in all)
 constexpr int kThreads = 32 * (kConsumers + 1);
 constexpr int kProducerWarp = kConsumers;
 constexpr int kDnRows = 4;                    // down rows per stage
@@ -57,6 +57,7 @@ struct Args {
     int nslots, ncons, nprod;
     uint32_t slot_bytes;
     int x_in_smem;            // tokens' rows staged in shared memory
+    int x_router_ring;        // no room for that: the router reads them from the (still idle) ring
     int do_combine;           // 0: leave Y for a separate combine kernel
     Workspace ws;
 };
@@ -102,7 +103,7 @@ __device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, vola
     __syncthreads();
     __shared__ int ok;
     if (threadIdx.x == 0) {
-        __threadfence();
+        fence_acq_rel_gpu();
         atomicAdd(ctr, 1u);
         ok = 1;
         unsigned long long t0 = global_ns();
@@ -114,7 +115,7 @@ __device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, vola
                 break;
             }
         }
-        __threadfence();
+        fence_acq_rel_gpu();
     }
     __syncthreads();
     return ok != 0;
@@ -151,7 +152,7 @@ __device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, in
 
 // Publish a warp's count of finished h rows (all lanes' h stores first).
 __device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
-    __threadfence();
+    fence_acq_rel_gpu();
     __syncwarp();
     if ((threadIdx.x & 31) == 0 && n) atomicAdd(ctr, (uint32_t)n);
 }
@@ -172,6 +173,26 @@ __device__ __forceinline__ bool wait_rows(const uint32_t *ctr, uint32_t target, 
         }
     }
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
+}
+
+// Sums of four rows' per-lane partials (one token), reduced together:
+// exchanging halves, lane group q (lanes 8q .. 8q+7) ends with row q, and its
+// first lane stores y[q] = sum * scale.
+__device__ __forceinline__ void store_four_rows(float r0, float r1, float r2, float r3, float *y, float scale) {
+    const int lane = threadIdx.x & 31;
+    const bool hi16 = lane & 16, hi8 = lane & 8;
+    // lanes < 16 keep rows 0,1; lanes >= 16 keep rows 2,3
+    float k0 = hi16 ? r2 : r0, k1 = hi16 ? r3 : r1;
+    const float s0 = hi16 ? r0 : r2, s1 = hi16 ? r1 : r3;
+    k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
+    k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
+    // within each half, lanes with bit 3 clear keep the first of the two rows
+    float k = hi8 ? k1 : k0;
+    k += __shfl_xor_sync(0xFFFFFFFFu, hi8 ? k0 : k1, 8);
+    k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
+    k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
+    k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
+    if ((lane & 7) == 0) y[lane >> 3] = k * scale;
 }
 
 // Per-warp cache of the expert a stage belongs to (read from shared memory).
@@ -199,50 +220,61 @@ __device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
     for (int r = 0; r < TM; ++r) s.tok[r] = r < s.n_e ? R.perm[s.row0 + r] : 0;
 }
 
-// top-k of one token by one warp, weights exp(l - lmax) / sum over the kept
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key; -0 is taken as +0 so that equal values tie). Key 0 lies below every
+// float and marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// top-k of one token by one warp, weights exp(l - lmax) / sum over the kept.
+// Lane l holds experts l, l + 32, ...; each pick is one warp-wide max of the
+// lanes' best keys and one warp-wide min of the ids that reach it (ties go to
+// the lower id).
 __device__ void topk_to_smem(const float *logits_row, int E, int k, int32_t *ids, float *w) {
     const int lane = threadIdx.x & 31;
-    float v[8];
+    uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        v[i] = e < E ? __ldcg(logits_row + e) : -INFINITY;
+        key[i] = e < E ? order_key(__ldcg(logits_row + e)) : 0u;
     }
-    uint32_t taken = 0;
-    float lmax = 0.f, sum = 0.f, my_val = 0.f;
+    uint32_t my_key = 0u;
     int my_id = 0;
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
+        // this lane's best: largest key, the lowest i (= lowest id) among equals
+        uint32_t bk = key[0];
+        int bi = 0;
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && !((taken >> i) & 1u) && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
-                bi = e;
+        for (int i = 1; i < 8; ++i)
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = i;
             }
-        }
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+        if ((int)(win & 31u) == lane) {
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            const int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
+            for (int i = 0; i < 8; ++i)
+                if (i == (int)(win >> 5)) key[i] = 0u;
         }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (j == 0) lmax = bv;
-        const float ex = expf(bv - lmax);
-        sum += ex;
         if (lane == j) {
-            my_val = ex;
-            my_id = bi;
+            my_key = m;
+            my_id = (int)win;
         }
     }
+    const float lmax = __shfl_sync(0xFFFFFFFFu, key_value(my_key), 0);
+    const float ex = lane < k ? expf(key_value(my_key) - lmax) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);  // picks in order, as a running sum
     if (lane < k) {
         ids[lane] = my_id;
-        w[lane] = my_val / sum;
+        w[lane] = ex / sum;
     }
 }
 
@@ -310,6 +342,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     unsigned char *xs = smem + 2048 + 8192;
     const uint32_t x_bytes = a.x_in_smem ? (uint32_t)T * d * 2 : 0u;
     unsigned char *ring = xs + ((x_bytes + 127) / 128) * 128;
+    // the router's copy of the tokens: the persistent one, or, before the
+    // weight stream starts, the ring
+    const uint32_t xr_bytes = (a.x_in_smem || a.x_router_ring) ? (uint32_t)T * d * 2 : 0u;
+    const unsigned char *xr = a.x_in_smem ? xs : ring;
 
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -322,9 +358,9 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     }
     for (int i = tid; i < 32; i += kThreads) cb_rows_s[i] = 0;
     __syncthreads();
-    if (tid == 32 * kProducerWarp && x_bytes) {
-        mbar_arrive_expect_tx(xbar, x_bytes);
-        bulk_g2s(xs, a.x, x_bytes, xbar, policy_evict_last());
+    if (tid == 32 * kProducerWarp && xr_bytes) {
+        mbar_arrive_expect_tx(xbar, xr_bytes);
+        bulk_g2s(const_cast<unsigned char *>(xr), a.x, xr_bytes, xbar, policy_evict_last());
     }
 
     // ---- 1. router: logits of this CTA's experts ----
@@ -332,7 +368,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     // four quarters of one expert's row
     {
         const int nq = d / 32;  // 16-byte vectors per quarter row (<= 256: at most 8 per lane)
-        bool x_ready = x_bytes == 0;
+        bool x_ready = xr_bytes == 0;
         for (int base = b; base < E; base += 2 * G) {
             const int eidx = base + (warp >= 4 ? G : 0);
             const int q = warp & 3;
@@ -361,8 +397,8 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
 #pragma unroll
                     for (int t = 0; t < TM; ++t) {
                         if (t < T) {
-                            const uint4 xv = a.x_in_smem
-                                                 ? reinterpret_cast<const uint4 *>(xs + (size_t)t * d * 2)[q * nq + v]
+                            const uint4 xv = xr_bytes
+                                                 ? reinterpret_cast<const uint4 *>(xr + (size_t)t * d * 2)[q * nq + v]
                                                  : __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * d) + q * nq + v);
                             float2 s2 = make_float2(0.f, 0.f);
                             s2 = ffma2(bf2(wv.x), bf2(xv.x), s2);
@@ -394,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
         }
         if (!x_ready) mbar_wait_or_abort(xbar, 0, err, abort_flag);  // CTAs without router rows
     }
-    grid_barrier(&ctrl->grid_bar, (uint32_t)G, err, abort_flag);
+    grid_barrier(&ctrl->grid_bar.v, (uint32_t)G, err, abort_flag);
 
     if (FP4 && x_bytes) {
         // NVFP4 gate/up sums in fp16: keep the staged tokens as fp16(x / max|x|)
@@ -423,20 +459,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     // ---- 2. routing, computed by every CTA in shared memory ----
     for (int t = warp; t < T; t += kConsumers + 1)
         topk_to_smem(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k);
-    for (int e = tid; e < E; e += kThreads) R.bm[e] = 0u;
-    __syncthreads();
-    for (int p = tid; p < T * k; p += kThreads) {
-        const int e = R.ids[p];
-        if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
-    }
-    __syncthreads();
-    for (int e = tid; e < E; e += kThreads) {
-        const int c = __popc(R.bm[e]);
-        R.cnt[e] = c;
-        R.scan[e] = c > 0;
-    }
-    __syncthreads();
+    if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
     if (warp == 0) {
+        // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
+        // tokens ascending within an expert
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) R.bm[e] = 0u;
+        __syncwarp();
+        for (int p = lane; p < T * k; p += 32) {
+            const int e = R.ids[p];
+            if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
+        }
+        __syncwarp();
+        for (int e = lane; e < E; e += 32) {
+            const int c = __popc(R.bm[e]);
+            R.cnt[e] = c;
+            R.scan[e] = c > 0;
+        }
+        __syncwarp();
         const int total = warp_scan256(R.cnt, R.off, E);
         __syncwarp();
         const int nu = warp_scan256(R.scan, R.scan, E);
@@ -447,14 +487,14 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             R.off[E] = total;
             *R.n_uniq = nu;
         }
-    }
-    __syncthreads();
-    for (int p = tid; p < T * k; p += kThreads) {
-        const int e = R.ids[p];
-        const int t = p / k;
-        const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
-        R.perm[row] = t;
-        R.pos[p] = row;
+        __syncwarp();
+        for (int p = lane; p < T * k; p += 32) {
+            const int e = R.ids[p];
+            const int t = p / k;
+            const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
+            R.perm[row] = t;
+            R.pos[p] = row;
+        }
     }
     __syncthreads();
     const int n_uniq = *R.n_uniq;
@@ -495,15 +535,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     if (warp == kProducerWarp) {
         // a.nprod lanes fill the ring, lane l the slots j with j % nprod == l
         // (nslots is a multiple of nprod), so every slot's fills come from one
-        // lane in order and the per-fill latency of a single issuing thread
-        // is overlapped nprod ways
+        // lane in order. The lanes poll their next slot without blocking and
+        // stay converged: a lane that sleeps in a blocking wait holds up the
+        // other lanes of its warp, whose slots may long be free.
         const int P = a.nprod;
-        if (lane < P && !*abort_flag) {
-            const uint64_t pol = policy_evict_first();
-            int s = lane;
-            for (; s < n_st; s += P) {
-                const int slot = s % NS;
-                if (s >= NS && !mbar_wait_or_abort(&empty[slot], ((s / NS) - 1) & 1, err, abort_flag)) break;
+        const uint64_t pol = policy_evict_first();
+        int s = lane;
+        unsigned long long t_progress = global_ns();
+        for (uint32_t it = 1;; ++it) {
+            const bool live = lane < P && s < n_st;
+            if (!__any_sync(0xFFFFFFFFu, live)) break;
+            const int slot = s % NS;
+            const bool ready = live && (s < NS || mbar_test_wait(&empty[slot], ((s / NS) - 1) & 1));
+            if (ready) {
                 unsigned char *dst = ring + (size_t)slot * a.slot_bytes;
                 if (s < n_gu) {
                     const int g = pl.gu_row(s);
@@ -533,10 +577,32 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                         bulk_g2s(dst + kDnRows * nq, a.sd + row * nsb, kDnRows * nsb, &full[slot], pol);
                     }
                 }
+                s += P;
             }
-            // every copy this lane issued must land before the CTA moves on
-            for (int j = lane; j < s; j += P)
-                if (j + NS >= s) mbar_wait(&full[j % NS], (j / NS) & 1, err);
+            // bounded: give up once no lane has issued for the wait limit
+            if (__any_sync(0xFFFFFFFFu, ready)) {
+                t_progress = 0;
+            } else if ((it & 255u) == 0) {
+                const unsigned long long now = global_ns();
+                if (t_progress == 0) t_progress = now;
+                const bool other_gave_up = *abort_flag != 0;
+                const bool timed_out = now - t_progress > kWaitLimitNs;
+                if (__any_sync(0xFFFFFFFFu, other_gave_up || timed_out)) {  // the whole warp leaves together
+                    if (lane == 0 && !other_gave_up) {
+                        atomicOr(err, ERRBIT_TIMEOUT);
+                        *abort_flag = 1;
+                    }
+                    break;
+                }
+            }
+        }
+        __syncwarp();
+        // every copy this lane issued must land before the CTA moves on (in a
+        // normal run the consumers have waited for all of them already)
+        if (lane < P) {
+            // the lane's last fill of each of its slots: stages s - NS .. s - P
+            // (s and NS - P are multiples of P apart from lane)
+            for (int j = max(lane, s - NS); j < s; j += P) mbar_wait(&full[j % NS], (j / NS) & 1, err);
         }
     } else if (warp < C) {
         // ------------------------------- gate/up -------------------------------
@@ -546,7 +612,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
         bool pub_a = false;
         for (; s < n_gu && !*abort_flag; s += C) {
             if (s >= pl.nA && !pub_a) {
-                publish_rows(&ctrl->h_ready[0], done_a);
+                publish_rows(&ctrl->h_ready[0].v, done_a);
                 pub_a = true;
             }
             if (s < pl.nA)
@@ -726,24 +792,24 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             }
         }
         // this warp's h rows are written: count them in
-        if (!pub_a) publish_rows(&ctrl->h_ready[0], done_a);
-        publish_rows(&ctrl->h_ready[1], done_b);
+        if (!pub_a) publish_rows(&ctrl->h_ready[0].v, done_a);
+        publish_rows(&ctrl->h_ready[1].v, done_b);
         bool ready_a = false, ready_b = false;
         // ---------------------------------- down ----------------------------------
         Seg<TM> sd;
         // an expert with one token: its h row stays in registers for all the
         // warp's stages of that expert (I <= 2048)
-        constexpr int kHC = TM <= 2 ? 8 : 1;
+        constexpr int kHC = 8;
         float4 hc0[kHC], hc1[kHC];
         int hc_u = -1;
         for (; s < n_st && !*abort_flag; s += C) {
             const int t = s - n_gu;
             if (t < pl.nC && !ready_a) {
-                if (!wait_rows(&ctrl->h_ready[0], (uint32_t)(U1 * I), err, abort_flag)) break;
+                if (!wait_rows(&ctrl->h_ready[0].v, (uint32_t)(U1 * I), err, abort_flag)) break;
                 ready_a = true;
             }
             if (t >= pl.nC && !ready_b) {
-                if (!wait_rows(&ctrl->h_ready[1], (uint32_t)((n_uniq - U1) * I), err, abort_flag)) break;
+                if (!wait_rows(&ctrl->h_ready[1].v, (uint32_t)((n_uniq - U1) * I), err, abort_flag)) break;
                 ready_b = true;
             }
             const int slot = s % NS;
@@ -753,163 +819,172 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
             const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
             const float *hrow = a.ws.h + (size_t)sd.row0 * I;
-            float2 acc[kDnRows][TM];
-#pragma unroll
-            for (int q = 0; q < kDnRows; ++q)
-#pragma unroll
-                for (int r = 0; r < TM; ++r) acc[q][r] = make_float2(0.f, 0.f);
-            if (!FP4) {
-                // token by token; h (in L2, written by other CTAs) fetched in
-                // chunks of kHV vectors per lane, all loads of a chunk issued
-                // before its arithmetic
-                constexpr int kHV = TM >= 8 ? 4 : 8;
-                const int nvec = I / 8;
-                if (TM <= 2 && sd.n_e == 1 && nvec <= 32 * kHC) {
-                    if (hc_u != sd.u) {
-                        const float4 *hr = reinterpret_cast<const float4 *>(hrow);
-#pragma unroll
-                        for (int jj = 0; jj < kHC; ++jj) {
-                            const int v = lane + 32 * jj;
-                            if (v < nvec) {
-                                hc0[jj] = __ldcg(hr + 2 * v);
-                                hc1[jj] = __ldcg(hr + 2 * v + 1);
-                            }
-                        }
-                        hc_u = sd.u;
-                    }
+            const float gsc = FP4 ? a.gd[sd.e] : 1.f;
+            const int nvec = I / 8;
+            if (!FP4 && sd.n_e == 1 && nvec <= 32 * kHC) {
+                // one token, its h row held in registers across the expert's stages
+                if (hc_u != sd.u) {
+                    const float4 *hr = reinterpret_cast<const float4 *>(hrow);
 #pragma unroll
                     for (int jj = 0; jj < kHC; ++jj) {
                         const int v = lane + 32 * jj;
                         if (v < nvec) {
-                            const float2 ha = make_float2(hc0[jj].x, hc0[jj].y), hb = make_float2(hc0[jj].z, hc0[jj].w);
-                            const float2 hc = make_float2(hc1[jj].x, hc1[jj].y), hd = make_float2(hc1[jj].z, hc1[jj].w);
-#pragma unroll
-                            for (int q = 0; q < kDnRows; ++q) {
-                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
-                                acc[q][0] = ffma2(bf2(wv.x), ha, acc[q][0]);
-                                acc[q][0] = ffma2(bf2(wv.y), hb, acc[q][0]);
-                                acc[q][0] = ffma2(bf2(wv.z), hc, acc[q][0]);
-                                acc[q][0] = ffma2(bf2(wv.w), hd, acc[q][0]);
-                            }
+                            hc0[jj] = __ldcg(hr + 2 * v);
+                            hc1[jj] = __ldcg(hr + 2 * v + 1);
                         }
                     }
-                } else
+                    hc_u = sd.u;
+                }
+                float2 acc[kDnRows];
 #pragma unroll
-                for (int r = 0; r < TM; ++r) {
-                    if (r < sd.n_e) {
-                        const float4 *hr = reinterpret_cast<const float4 *>(hrow + (size_t)r * I);
-                        for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
-                            float4 h0[kHV], h1[kHV];
+                for (int q = 0; q < kDnRows; ++q) acc[q] = make_float2(0.f, 0.f);
 #pragma unroll
-                            for (int jj = 0; jj < kHV; ++jj) {
-                                const int v = lane + 32 * (j0 + jj);
-                                if (v < nvec) {
-                                    h0[jj] = __ldcg(hr + 2 * v);
-                                    h1[jj] = __ldcg(hr + 2 * v + 1);
+                for (int jj = 0; jj < kHC; ++jj) {
+                    const int v = lane + 32 * jj;
+                    if (v < nvec) {
+                        const float2 ha = make_float2(hc0[jj].x, hc0[jj].y), hb = make_float2(hc0[jj].z, hc0[jj].w);
+                        const float2 hc = make_float2(hc1[jj].x, hc1[jj].y), hd = make_float2(hc1[jj].z, hc1[jj].w);
+#pragma unroll
+                        for (int q = 0; q < kDnRows; ++q) {
+                            const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                            acc[q] = ffma2(bf2(wv.x), ha, acc[q]);
+                            acc[q] = ffma2(bf2(wv.y), hb, acc[q]);
+                            acc[q] = ffma2(bf2(wv.z), hc, acc[q]);
+                            acc[q] = ffma2(bf2(wv.w), hd, acc[q]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                store_four_rows(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y, acc[3].x + acc[3].y,
+                                a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
+            } else {
+                // the expert's tokens in groups of up to TG (bounded registers)
+                constexpr int TG = TM < 8 ? TM : 8;
+                for (int r0 = 0; r0 < sd.n_e; r0 += TG) {
+                    const int nr = min(TG, sd.n_e - r0);
+                    const float *hg = hrow + (size_t)r0 * I;
+                    float2 acc[kDnRows][TG];
+#pragma unroll
+                    for (int q = 0; q < kDnRows; ++q)
+#pragma unroll
+                        for (int r = 0; r < TG; ++r) acc[q][r] = make_float2(0.f, 0.f);
+                    if (!FP4) {
+                        // token by token; h (in L2, written by other CTAs) fetched
+                        // in chunks of kHV vectors per lane, all loads of a chunk
+                        // issued before its arithmetic
+                        constexpr int kHV = TG >= 8 ? 4 : 8;
+#pragma unroll
+                        for (int r = 0; r < TG; ++r) {
+                            if (r < nr) {
+                                const float4 *hr = reinterpret_cast<const float4 *>(hg + (size_t)r * I);
+                                for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
+                                    float4 h0[kHV], h1[kHV];
+#pragma unroll
+                                    for (int jj = 0; jj < kHV; ++jj) {
+                                        const int v = lane + 32 * (j0 + jj);
+                                        if (v < nvec) {
+                                            h0[jj] = __ldcg(hr + 2 * v);
+                                            h1[jj] = __ldcg(hr + 2 * v + 1);
+                                        }
+                                    }
+#pragma unroll
+                                    for (int jj = 0; jj < kHV; ++jj) {
+                                        const int v = lane + 32 * (j0 + jj);
+                                        if (v < nvec) {
+                                            const float2 ha = make_float2(h0[jj].x, h0[jj].y);
+                                            const float2 hb = make_float2(h0[jj].z, h0[jj].w);
+                                            const float2 hc = make_float2(h1[jj].x, h1[jj].y);
+                                            const float2 hd = make_float2(h1[jj].z, h1[jj].w);
+#pragma unroll
+                                            for (int q = 0; q < kDnRows; ++q) {
+                                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                                                acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
+                                                acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
+                                                acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
+                                                acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
+                                            }
+                                        }
+                                    }
                                 }
                             }
+                        }
+                    } else {
+                        const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
+                        for (int bb = lane; bb < I / 16; bb += 32) {
 #pragma unroll
-                            for (int jj = 0; jj < kHV; ++jj) {
-                                const int v = lane + 32 * (j0 + jj);
-                                if (v < nvec) {
-                                    const float2 ha = make_float2(h0[jj].x, h0[jj].y), hb = make_float2(h0[jj].z, h0[jj].w);
-                                    const float2 hc = make_float2(h1[jj].x, h1[jj].y), hd = make_float2(h1[jj].z, h1[jj].w);
+                            for (int q = 0; q < kDnRows; ++q) {
+                                float2 wf[8];
+                                fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
+                                const float sc = e4m3f(sb[q * (I / 16) + bb]);
 #pragma unroll
-                                    for (int q = 0; q < kDnRows; ++q) {
-                                        const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
-                                        acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
-                                        acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
-                                        acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
-                                        acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
+                                for (int r = 0; r < TG; ++r) {
+                                    if (r < nr) {
+                                        const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
+                                        float2 p = make_float2(0.f, 0.f);
+#pragma unroll
+                                        for (int h4 = 0; h4 < 4; ++h4) {
+                                            const float4 hv = __ldcg(hp + h4);
+                                            p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
+                                            p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
+                                        }
+                                        acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
                                     }
                                 }
                             }
                         }
                     }
-                }
-            } else {
-                const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
-                for (int bb = lane; bb < I / 16; bb += 32) {
+                    if (nr == 1) {
+                        store_four_rows(acc[0][0].x + acc[0][0].y, acc[1][0].x + acc[1][0].y,
+                                        acc[2][0].x + acc[2][0].y, acc[3][0].x + acc[3][0].y,
+                                        a.ws.Y + (size_t)(sd.row0 + r0) * d + c0, gsc);
+                    } else {
 #pragma unroll
-                    for (int q = 0; q < kDnRows; ++q) {
-                        float2 wf[8];
-                        fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
-                        const float sc = e4m3f(sb[q * (I / 16) + bb]);
+                        for (int q = 0; q < kDnRows; ++q) {
+                            float yv = 0.f;
 #pragma unroll
-                        for (int r = 0; r < TM; ++r) {
-                            if (r < sd.n_e) {
-                                const float4 *hp = reinterpret_cast<const float4 *>(hrow + (size_t)r * I + bb * 16);
-                                float2 p = make_float2(0.f, 0.f);
-#pragma unroll
-                                for (int h4 = 0; h4 < 4; ++h4) {
-                                    const float4 hv = __ldcg(hp + h4);
-                                    p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
-                                    p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
+                            for (int r = 0; r < TG; ++r) {
+                                if (r < nr) {
+                                    const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
+                                    if (lane == r) yv = sum * gsc;
                                 }
-                                acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
                             }
+                            if (lane < nr) a.ws.Y[(size_t)(sd.row0 + r0 + lane) * d + c0 + q] = yv;
                         }
                     }
                 }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            const float gsc = FP4 ? a.gd[sd.e] : 1.f;
-            if (sd.n_e == 1) {
-                // one token: reduce the four rows' partial sums together,
-                // exchanging halves so that lane group q ends with row q
-                static_assert(kDnRows == 4, "the transposed reduction takes four rows");
-                float r0 = acc[0][0].x + acc[0][0].y, r1 = acc[1][0].x + acc[1][0].y;
-                float r2 = acc[2][0].x + acc[2][0].y, r3 = acc[3][0].x + acc[3][0].y;
-                const bool hi16 = lane & 16, hi8 = lane & 8;
-                // step 1: lanes < 16 keep rows 0,1; lanes >= 16 keep rows 2,3
-                float k0 = hi16 ? r2 : r0, k1 = hi16 ? r3 : r1;
-                const float s0 = hi16 ? r0 : r2, s1 = hi16 ? r1 : r3;
-                k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
-                k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
-                // step 2: within each half, lanes with bit 3 clear keep the first row
-                float k = hi8 ? k1 : k0;
-                k += __shfl_xor_sync(0xFFFFFFFFu, hi8 ? k0 : k1, 8);
-                k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
-                k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
-                k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
-                // lane groups of 8: [0,8) row 0, [8,16) row 1, [16,24) row 2, [24,32) row 3
-                if ((lane & 7) == 0) a.ws.Y[(size_t)sd.row0 * d + c0 + (lane >> 3)] = k * gsc;
-            } else {
-#pragma unroll
-                for (int q = 0; q < kDnRows; ++q) {
-                    float yv = 0.f;
-#pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < sd.n_e) {
-                            const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
-                            if (lane == r) yv = sum * gsc;
-                        }
-                    }
-                    if (lane < sd.n_e) a.ws.Y[(size_t)(sd.row0 + lane) * d + c0 + q] = yv;
-                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
             }
             if (lane == 0) atomicAdd(&cb_rows_s[c0 / kCb], kDnRows);
         }
     }
 
     // ---- 5. combine, by the CTA that completes each column block ----
-    __threadfence();  // this thread's h and Y stores before the block's count below
+    fence_acq_rel_gpu();  // this thread's h and Y stores before the block's count below
     __syncthreads();
     if (a.do_combine) {
-        if (tid == 0) {
-            int n = 0;
-            __threadfence();
+        if (warp == 0) {
+            // lane cb counts this CTA's rows of column block cb in; the
+            // counts go out together rather than one round trip after another
             const int ncb = (d + kCb - 1) / kCb;
-            for (int cb = 0; cb < ncb; ++cb) {
-                const int mine = cb_rows_s[cb];
-                if (!mine) continue;
-                const int cols = min(kCb, d - cb * kCb);
-                const uint32_t done = atomicAdd(&ctrl->cb_rows[cb], (uint32_t)mine) + mine;
-                if (done == (uint32_t)(n_uniq * cols)) cb_todo[n++] = cb;
+            bool fin = false;
+            fence_acq_rel_gpu();  // the CTA's stores (ordered by the barrier) before this lane's count
+            if (lane < ncb) {
+                const int mine = cb_rows_s[lane];
+                if (mine) {
+                    const int cols = min(kCb, d - lane * kCb);
+                    const uint32_t done = atomicAdd(&ctrl->cb_rows[lane].v, (uint32_t)mine) + mine;
+                    fin = done == (uint32_t)(n_uniq * cols);
+                }
             }
-            *n_todo = n;
-            __threadfence();
+            fence_acq_rel_gpu();
+            const uint32_t fin_mask = __ballot_sync(0xFFFFFFFFu, fin);
+            if (lane == 0) {
+                int n = 0;
+                for (uint32_t m = fin_mask; m; m &= m - 1) cb_todo[n++] = __ffs(m) - 1;
+                *n_todo = n;
+            }
         }
         __syncthreads();
         for (int ti = 0; ti < *n_todo; ++ti) {
@@ -939,20 +1014,20 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                 o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
                 *reinterpret_cast<uint2 *>(a.out + (size_t)t * d + c) = o;
             }
-            if (tid == 0) ctrl->cb_rows[cb] = 0u;
+            if (tid == 0) ctrl->cb_rows[cb].v = 0u;
         }
     }
     // ---- exit: the last CTA out resets the grid-barrier counters ----
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
-        if (atomicAdd(&ctrl->grid_exit, 1u) == (uint32_t)G - 1) {
-            for (int cb = 0; cb < 32; ++cb) ctrl->cb_rows[cb] = 0u;  // zero already unless a wait gave up
-            ctrl->grid_bar = 0u;
-            ctrl->h_ready[0] = 0u;
-            ctrl->h_ready[1] = 0u;
-            ctrl->grid_exit = 0u;
-            __threadfence();
+        fence_acq_rel_gpu();
+        if (atomicAdd(&ctrl->grid_exit.v, 1u) == (uint32_t)G - 1) {
+            for (int cb = 0; cb < 32; ++cb) ctrl->cb_rows[cb].v = 0u;  // zero already unless a wait gave up
+            ctrl->grid_bar.v = 0u;
+            ctrl->h_ready[0].v = 0u;
+            ctrl->h_ready[1].v = 0u;
+            ctrl->grid_exit.v = 0u;
+            fence_acq_rel_gpu();
         }
     }
 }
@@ -1010,6 +1085,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     if (fixed + xb2 + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
     const int fit = (int)((kSmemBudget - fixed - xb2) / a.slot_bytes);
     a.nslots = pick<FP4>(fit, a.ncons);
+    a.x_router_ring = !a.x_in_smem && (size_t)a.nslots * a.slot_bytes >= (size_t)T * L.d * 2 ? 1 : 0;
     a.nprod = a.nslots % 4 == 0 ? 4 : (a.nslots % 2 == 0 ? 2 : 1);
     const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
     static bool attr = false;
