@@ -304,6 +304,282 @@ __device__ int warp_scan256(const int32_t *a, int32_t *out, int n) {
     return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
+// One gate/up stage (the row pair i of expert seg.e in `st`) for an expert
+// with NE tokens at most (seg.n_e <= NE; exactly NE when NE <= 2): h rows of
+// its tokens, h = silu(g) * u. Releases the slot once the stage is read.
+template <int NE, int TM, bool FP4>
+__device__ __forceinline__ void gu_stage(const Args &a, const unsigned char *st, const unsigned char *xs,
+                                         const float *xscale, const Seg<TM> &seg, uint64_t *empty_slot, int i) {
+    const int lane = threadIdx.x & 31;
+    const int d = a.d, I = a.I;
+    const uint32_t rbg = rowb<FP4>(d);
+    float2 ag[NE], au[NE];
+#pragma unroll
+    for (int r = 0; r < NE; ++r) ag[r] = au[r] = make_float2(0.f, 0.f);
+    if (!FP4) {
+        constexpr int kXV = 8;
+        const uint4 *gw = reinterpret_cast<const uint4 *>(st);
+        const uint4 *uw = reinterpret_cast<const uint4 *>(st + rbg);
+        const int nvec = d / 8;
+        if (a.x_in_smem) {
+            // vector by vector: each weight vector is unpacked once and
+            // used for every token of the expert
+#pragma unroll 2
+            for (int v = lane; v < nvec; v += 32) {
+                const uint4 g4 = gw[v], u4 = uw[v];
+                const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
+                const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
+#pragma unroll
+                for (int r = 0; r < NE; ++r) {
+                    if (NE <= 2 || r < seg.n_e) {
+                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v];
+                        const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
+                        ag[r] = ffma2(g0, x0, ag[r]);
+                        au[r] = ffma2(u0, x0, au[r]);
+                        ag[r] = ffma2(g1, x1, ag[r]);
+                        au[r] = ffma2(u1, x1, au[r]);
+                        ag[r] = ffma2(g2, x2, ag[r]);
+                        au[r] = ffma2(u2, x2, au[r]);
+                        ag[r] = ffma2(g3, x3, ag[r]);
+                        au[r] = ffma2(u3, x3, au[r]);
+                    }
+                }
+            }
+        } else {
+        // token by token; each lane's vectors in chunks of kXV whose
+        // token loads (from global memory) are all issued before the
+        // arithmetic: one latency per chunk
+#pragma unroll
+        for (int r = 0; r < NE; ++r) {
+            if (NE <= 2 || r < seg.n_e) {
+                const uint4 *xrow = a.x_in_smem
+                                        ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)
+                                        : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d);
+                for (int j0 = 0; j0 * 32 < nvec; j0 += kXV) {
+                    uint4 xv[kXV];
+#pragma unroll
+                    for (int jj = 0; jj < kXV; ++jj) {
+                        const int v = lane + 32 * (j0 + jj);
+                        xv[jj] = v < nvec ? (a.x_in_smem ? xrow[v] : __ldg(xrow + v)) : make_uint4(0, 0, 0, 0);
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < kXV; ++jj) {
+                        const int v = lane + 32 * (j0 + jj);
+                        if (v < nvec) {
+                            const uint4 g4 = gw[v], u4 = uw[v];
+                            const float2 x0 = bf2(xv[jj].x), x1 = bf2(xv[jj].y), x2 = bf2(xv[jj].z),
+                                         x3 = bf2(xv[jj].w);
+                            ag[r] = ffma2(bf2(g4.x), x0, ag[r]);
+                            au[r] = ffma2(bf2(u4.x), x0, au[r]);
+                            ag[r] = ffma2(bf2(g4.y), x1, ag[r]);
+                            au[r] = ffma2(bf2(u4.y), x1, au[r]);
+                            ag[r] = ffma2(bf2(g4.z), x2, ag[r]);
+                            au[r] = ffma2(bf2(u4.z), x2, au[r]);
+                            ag[r] = ffma2(bf2(g4.w), x3, ag[r]);
+                            au[r] = ffma2(bf2(u4.w), x3, au[r]);
+                        }
+                    }
+                }
+            }
+        }
+        }
+    } else {
+        const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rbg, *us = st + rbg + d / 2;
+        if (a.x_in_smem) {
+            // tokens in shared memory as fp16(x / max|x|): the 16 products
+            // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
+            // pairs, then scaled by the block scale and max|x| in fp32
+            for (int bb = lane; bb < d / 16; bb += 32) {
+                const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
+                const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
+                __half2 gh[8], uh[8];
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const uint32_t gw_ = q < 4 ? gqv.x : gqv.y, uw_ = q < 4 ? uqv.x : uqv.y;
+                    __half2_raw g2 = __nv_cvt_fp4x2_to_halfraw2(
+                        (__nv_fp4x2_storage_t)((gw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
+                    __half2_raw u2 = __nv_cvt_fp4x2_to_halfraw2(
+                        (__nv_fp4x2_storage_t)((uw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
+                    gh[q] = *reinterpret_cast<__half2 *>(&g2);
+                    uh[q] = *reinterpret_cast<__half2 *>(&u2);
+                }
+                const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
+#pragma unroll
+                for (int r = 0; r < NE; ++r) {
+                    if (NE <= 2 || r < seg.n_e) {
+                        const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2;
+                        const uint4 xa = xp[0], xb = xp[1];
+                        const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                        __half2 pg = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+                        __half2 pu = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+#pragma unroll
+                        for (int q = 1; q < 8; ++q) {
+                            pg = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg);
+                            pu = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu);
+                        }
+                        const float2 fg = __half22float2(pg), fu = __half22float2(pu);
+                        const float xsc = xscale[seg.tok[r]];
+                        ag[r].x = fmaf(fg.x + fg.y, sgb * xsc, ag[r].x);
+                        au[r].x = fmaf(fu.x + fu.y, sub * xsc, au[r].x);
+                    }
+                }
+            }
+        } else
+        for (int bb = lane; bb < d / 16; bb += 32) {
+            float2 gf[8], uf[8];
+            fp4x16(*reinterpret_cast<const uint2 *>(gq + bb * 8), gf);
+            fp4x16(*reinterpret_cast<const uint2 *>(uq + bb * 8), uf);
+            const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
+#pragma unroll
+            for (int r = 0; r < NE; ++r) {
+                if (NE <= 2 || r < seg.n_e) {
+                    const uint4 *xp =
+                        a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2
+                                    : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + bb * 2;
+                    const uint4 xa = a.x_in_smem ? xp[0] : __ldg(xp), xb = a.x_in_smem ? xp[1] : __ldg(xp + 1);
+                    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
+                    float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float2 xq = bf2(xw[q]);
+                        pg = ffma2(gf[q], xq, pg);
+                        pu = ffma2(uf[q], xq, pu);
+                    }
+                    ag[r].x = fmaf(pg.x + pg.y, sgb, ag[r].x);
+                    au[r].x = fmaf(pu.x + pu.y, sub, au[r].x);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_slot);
+    const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
+    if (seg.n_e == 1) {
+        // one token: lanes < 16 reduce the gate sum, lanes >= 16 the up sum
+        const bool hi = lane & 16;
+        const float gs_ = ag[0].x + ag[0].y, us_ = au[0].x + au[0].y;
+        float kk = hi ? us_ : gs_;
+        kk += __shfl_xor_sync(0xFFFFFFFFu, hi ? gs_ : us_, 16);
+        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 8);
+        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
+        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
+        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
+        const float up_total = __shfl_sync(0xFFFFFFFFu, kk, 16);
+        if (lane == 0) a.ws.h[(size_t)seg.row0 * I + i] = silu(kk * gsc) * (up_total * usc);
+    } else {
+        float hv = 0.f;
+#pragma unroll
+        for (int r = 0; r < NE; ++r) {
+            if (NE <= 2 || r < seg.n_e) {
+                const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
+                const float su_ = warp_sum(au[r].x + au[r].y) * usc;
+                if (lane == r) hv = silu(sg_) * su_;
+            }
+        }
+        if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
+    }
+}
+
+// Down rows of one stage (kDnRows rows of W_down in `st`) for a group of nr
+// tokens of one expert (nr <= NG; exactly NG when NG <= 2), h rows at hg:
+// y[t][q] for the group's tokens t, stored at yg[t * d + q] (scaled by gsc).
+template <int NG, bool FP4>
+__device__ __forceinline__ void dn_group(const Args &a, const unsigned char *st, const float *hg, int nr, float *yg,
+                                         float gsc) {
+    const int lane = threadIdx.x & 31;
+    const int d = a.d, I = a.I;
+    const int nvec = I / 8;
+    const uint32_t rbd = rowb<FP4>(I);
+    float2 acc[kDnRows][NG];
+#pragma unroll
+    for (int q = 0; q < kDnRows; ++q)
+#pragma unroll
+        for (int r = 0; r < NG; ++r) acc[q][r] = make_float2(0.f, 0.f);
+    if (!FP4) {
+        // token by token; h (in L2, written by other CTAs) fetched
+        // in chunks of kHV vectors per lane, all loads of a chunk
+        // issued before its arithmetic
+        constexpr int kHV = 4;
+#pragma unroll
+        for (int r = 0; r < NG; ++r) {
+            if (NG <= 2 || r < nr) {
+                const float4 *hr = reinterpret_cast<const float4 *>(hg + (size_t)r * I);
+                for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
+                    float4 h0[kHV], h1[kHV];
+#pragma unroll
+                    for (int jj = 0; jj < kHV; ++jj) {
+                        const int v = lane + 32 * (j0 + jj);
+                        if (v < nvec) {
+                            h0[jj] = __ldcg(hr + 2 * v);
+                            h1[jj] = __ldcg(hr + 2 * v + 1);
+                        }
+                    }
+#pragma unroll
+                    for (int jj = 0; jj < kHV; ++jj) {
+                        const int v = lane + 32 * (j0 + jj);
+                        if (v < nvec) {
+                            const float2 ha = make_float2(h0[jj].x, h0[jj].y);
+                            const float2 hb = make_float2(h0[jj].z, h0[jj].w);
+                            const float2 hc = make_float2(h1[jj].x, h1[jj].y);
+                            const float2 hd = make_float2(h1[jj].z, h1[jj].w);
+#pragma unroll
+                            for (int q = 0; q < kDnRows; ++q) {
+                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
+                                acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
+                                acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    } else {
+        const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
+        for (int bb = lane; bb < I / 16; bb += 32) {
+#pragma unroll
+            for (int q = 0; q < kDnRows; ++q) {
+                float2 wf[8];
+                fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
+                const float sc = e4m3f(sb[q * (I / 16) + bb]);
+#pragma unroll
+                for (int r = 0; r < NG; ++r) {
+                    if (NG <= 2 || r < nr) {
+                        const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
+                        float2 p = make_float2(0.f, 0.f);
+#pragma unroll
+                        for (int h4 = 0; h4 < 4; ++h4) {
+                            const float4 hv = __ldcg(hp + h4);
+                            p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
+                            p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
+                        }
+                        acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
+                    }
+                }
+            }
+        }
+    }
+    if (nr == 1) {
+        store_four_rows(acc[0][0].x + acc[0][0].y, acc[1][0].x + acc[1][0].y,
+                        acc[2][0].x + acc[2][0].y, acc[3][0].x + acc[3][0].y,
+                        yg, gsc);
+    } else {
+#pragma unroll
+        for (int q = 0; q < kDnRows; ++q) {
+            float yv = 0.f;
+#pragma unroll
+            for (int r = 0; r < NG; ++r) {
+                if (NG <= 2 || r < nr) {
+                    const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
+                    if (lane == r) yv = sum * gsc;
+                }
+            }
+            if (lane < nr) yg[(size_t)lane * d + q] = yv;
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------
@@ -625,171 +901,16 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
             if (u != seg.u) seg_load(seg, R, u);
             if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
             const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
-            float2 ag[TM], au[TM];
-#pragma unroll
-            for (int r = 0; r < TM; ++r) ag[r] = au[r] = make_float2(0.f, 0.f);
-            if (!FP4) {
-                constexpr int kXV = 8;
-                const uint4 *gw = reinterpret_cast<const uint4 *>(st);
-                const uint4 *uw = reinterpret_cast<const uint4 *>(st + rbg);
-                const int nvec = d / 8;
-                if (a.x_in_smem) {
-                    // vector by vector: each weight vector is unpacked once and
-                    // used for every token of the expert
-#pragma unroll 2
-                    for (int v = lane; v < nvec; v += 32) {
-                        const uint4 g4 = gw[v], u4 = uw[v];
-                        const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
-                        const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
-#pragma unroll
-                        for (int r = 0; r < TM; ++r) {
-                            if (r < seg.n_e) {
-                                const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v];
-                                const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
-                                ag[r] = ffma2(g0, x0, ag[r]);
-                                au[r] = ffma2(u0, x0, au[r]);
-                                ag[r] = ffma2(g1, x1, ag[r]);
-                                au[r] = ffma2(u1, x1, au[r]);
-                                ag[r] = ffma2(g2, x2, ag[r]);
-                                au[r] = ffma2(u2, x2, au[r]);
-                                ag[r] = ffma2(g3, x3, ag[r]);
-                                au[r] = ffma2(u3, x3, au[r]);
-                            }
-                        }
-                    }
-                } else {
-                // token by token; each lane's vectors in chunks of kXV whose
-                // token loads (from global memory) are all issued before the
-                // arithmetic: one latency per chunk
-#pragma unroll
-                for (int r = 0; r < TM; ++r) {
-                    if (r < seg.n_e) {
-                        const uint4 *xrow = a.x_in_smem
-                                                ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)
-                                                : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d);
-                        for (int j0 = 0; j0 * 32 < nvec; j0 += kXV) {
-                            uint4 xv[kXV];
-#pragma unroll
-                            for (int jj = 0; jj < kXV; ++jj) {
-                                const int v = lane + 32 * (j0 + jj);
-                                xv[jj] = v < nvec ? (a.x_in_smem ? xrow[v] : __ldg(xrow + v)) : make_uint4(0, 0, 0, 0);
-                            }
-#pragma unroll
-                            for (int jj = 0; jj < kXV; ++jj) {
-                                const int v = lane + 32 * (j0 + jj);
-                                if (v < nvec) {
-                                    const uint4 g4 = gw[v], u4 = uw[v];
-                                    const float2 x0 = bf2(xv[jj].x), x1 = bf2(xv[jj].y), x2 = bf2(xv[jj].z),
-                                                 x3 = bf2(xv[jj].w);
-                                    ag[r] = ffma2(bf2(g4.x), x0, ag[r]);
-                                    au[r] = ffma2(bf2(u4.x), x0, au[r]);
-                                    ag[r] = ffma2(bf2(g4.y), x1, ag[r]);
-                                    au[r] = ffma2(bf2(u4.y), x1, au[r]);
-                                    ag[r] = ffma2(bf2(g4.z), x2, ag[r]);
-                                    au[r] = ffma2(bf2(u4.z), x2, au[r]);
-                                    ag[r] = ffma2(bf2(g4.w), x3, ag[r]);
-                                    au[r] = ffma2(bf2(u4.w), x3, au[r]);
-                                }
-                            }
-                        }
-                    }
-                }
-                }
-            } else {
-                const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rbg, *us = st + rbg + d / 2;
-                if (a.x_in_smem) {
-                    // tokens in shared memory as fp16(x / max|x|): the 16 products
-                    // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
-                    // pairs, then scaled by the block scale and max|x| in fp32
-                    for (int bb = lane; bb < d / 16; bb += 32) {
-                        const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
-                        const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
-                        __half2 gh[8], uh[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) {
-                            const uint32_t gw_ = q < 4 ? gqv.x : gqv.y, uw_ = q < 4 ? uqv.x : uqv.y;
-                            __half2_raw g2 = __nv_cvt_fp4x2_to_halfraw2(
-                                (__nv_fp4x2_storage_t)((gw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                            __half2_raw u2 = __nv_cvt_fp4x2_to_halfraw2(
-                                (__nv_fp4x2_storage_t)((uw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                            gh[q] = *reinterpret_cast<__half2 *>(&g2);
-                            uh[q] = *reinterpret_cast<__half2 *>(&u2);
-                        }
-                        const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
-#pragma unroll
-                        for (int r = 0; r < TM; ++r) {
-                            if (r < seg.n_e) {
-                                const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2;
-                                const uint4 xa = xp[0], xb = xp[1];
-                                const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                                __half2 pg = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
-                                __half2 pu = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
-#pragma unroll
-                                for (int q = 1; q < 8; ++q) {
-                                    pg = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg);
-                                    pu = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu);
-                                }
-                                const float2 fg = __half22float2(pg), fu = __half22float2(pu);
-                                const float xsc = xscale[seg.tok[r]];
-                                ag[r].x = fmaf(fg.x + fg.y, sgb * xsc, ag[r].x);
-                                au[r].x = fmaf(fu.x + fu.y, sub * xsc, au[r].x);
-                            }
-                        }
-                    }
-                } else
-                for (int bb = lane; bb < d / 16; bb += 32) {
-                    float2 gf[8], uf[8];
-                    fp4x16(*reinterpret_cast<const uint2 *>(gq + bb * 8), gf);
-                    fp4x16(*reinterpret_cast<const uint2 *>(uq + bb * 8), uf);
-                    const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
-#pragma unroll
-                    for (int r = 0; r < TM; ++r) {
-                        if (r < seg.n_e) {
-                            const uint4 *xp =
-                                a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2
-                                            : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + bb * 2;
-                            const uint4 xa = a.x_in_smem ? xp[0] : __ldg(xp), xb = a.x_in_smem ? xp[1] : __ldg(xp + 1);
-                            const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                            float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const float2 xq = bf2(xw[q]);
-                                pg = ffma2(gf[q], xq, pg);
-                                pu = ffma2(uf[q], xq, pu);
-                            }
-                            ag[r].x = fmaf(pg.x + pg.y, sgb, ag[r].x);
-                            au[r].x = fmaf(pu.x + pu.y, sub, au[r].x);
-                        }
-                    }
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
-            const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
-            if (seg.n_e == 1) {
-                // one token: lanes < 16 reduce the gate sum, lanes >= 16 the up sum
-                const bool hi = lane & 16;
-                const float gs_ = ag[0].x + ag[0].y, us_ = au[0].x + au[0].y;
-                float kk = hi ? us_ : gs_;
-                kk += __shfl_xor_sync(0xFFFFFFFFu, hi ? gs_ : us_, 16);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 8);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
-                kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
-                const float up_total = __shfl_sync(0xFFFFFFFFu, kk, 16);
-                if (lane == 0) a.ws.h[(size_t)seg.row0 * I + i] = silu(kk * gsc) * (up_total * usc);
-            } else {
-                float hv = 0.f;
-#pragma unroll
-                for (int r = 0; r < TM; ++r) {
-                    if (r < seg.n_e) {
-                        const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
-                        const float su_ = warp_sum(au[r].x + au[r].y) * usc;
-                        if (lane == r) hv = silu(sg_) * su_;
-                    }
-                }
-                if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
-            }
+            if (TM == 1 || seg.n_e == 1)
+                gu_stage<1, TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
+            else if (TM == 2 || seg.n_e == 2)
+                gu_stage<(TM < 2 ? TM : 2), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
+            else if (TM == 4 || seg.n_e <= 4)
+                gu_stage<(TM < 4 ? TM : 4), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
+            else if (TM == 8 || seg.n_e <= 8)
+                gu_stage<(TM < 8 ? TM : 8), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
+            else
+                gu_stage<TM, TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
         }
         // this warp's h rows are written: count them in
         if (!pub_a) publish_rows(&ctrl->h_ready[0].v, done_a);
@@ -860,98 +981,19 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                                 a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
             } else {
                 // the expert's tokens in groups of up to TG (bounded registers)
-                constexpr int TG = TM < 8 ? TM : 8;
+                constexpr int TG = TM < 4 ? TM : 4;
                 for (int r0 = 0; r0 < sd.n_e; r0 += TG) {
                     const int nr = min(TG, sd.n_e - r0);
                     const float *hg = hrow + (size_t)r0 * I;
-                    float2 acc[kDnRows][TG];
-#pragma unroll
-                    for (int q = 0; q < kDnRows; ++q)
-#pragma unroll
-                        for (int r = 0; r < TG; ++r) acc[q][r] = make_float2(0.f, 0.f);
-                    if (!FP4) {
-                        // token by token; h (in L2, written by other CTAs) fetched
-                        // in chunks of kHV vectors per lane, all loads of a chunk
-                        // issued before its arithmetic
-                        constexpr int kHV = TG >= 8 ? 4 : 8;
-#pragma unroll
-                        for (int r = 0; r < TG; ++r) {
-                            if (r < nr) {
-                                const float4 *hr = reinterpret_cast<const float4 *>(hg + (size_t)r * I);
-                                for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
-                                    float4 h0[kHV], h1[kHV];
-#pragma unroll
-                                    for (int jj = 0; jj < kHV; ++jj) {
-                                        const int v = lane + 32 * (j0 + jj);
-                                        if (v < nvec) {
-                                            h0[jj] = __ldcg(hr + 2 * v);
-                                            h1[jj] = __ldcg(hr + 2 * v + 1);
-                                        }
-                                    }
-#pragma unroll
-                                    for (int jj = 0; jj < kHV; ++jj) {
-                                        const int v = lane + 32 * (j0 + jj);
-                                        if (v < nvec) {
-                                            const float2 ha = make_float2(h0[jj].x, h0[jj].y);
-                                            const float2 hb = make_float2(h0[jj].z, h0[jj].w);
-                                            const float2 hc = make_float2(h1[jj].x, h1[jj].y);
-                                            const float2 hd = make_float2(h1[jj].z, h1[jj].w);
-#pragma unroll
-                                            for (int q = 0; q < kDnRows; ++q) {
-                                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
-                                                acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
-                                                acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
-                                                acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
-                                                acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
-                                            }
-                                        }
-                                    }
-                                }
-                            }
-                        }
-                    } else {
-                        const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
-                        for (int bb = lane; bb < I / 16; bb += 32) {
-#pragma unroll
-                            for (int q = 0; q < kDnRows; ++q) {
-                                float2 wf[8];
-                                fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
-                                const float sc = e4m3f(sb[q * (I / 16) + bb]);
-#pragma unroll
-                                for (int r = 0; r < TG; ++r) {
-                                    if (r < nr) {
-                                        const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
-                                        float2 p = make_float2(0.f, 0.f);
-#pragma unroll
-                                        for (int h4 = 0; h4 < 4; ++h4) {
-                                            const float4 hv = __ldcg(hp + h4);
-                                            p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
-                                            p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
-                                        }
-                                        acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
-                                    }
-                                }
-                            }
-                        }
-                    }
-                    if (nr == 1) {
-                        store_four_rows(acc[0][0].x + acc[0][0].y, acc[1][0].x + acc[1][0].y,
-                                        acc[2][0].x + acc[2][0].y, acc[3][0].x + acc[3][0].y,
-                                        a.ws.Y + (size_t)(sd.row0 + r0) * d + c0, gsc);
-                    } else {
-#pragma unroll
-                        for (int q = 0; q < kDnRows; ++q) {
-                            float yv = 0.f;
-#pragma unroll
-                            for (int r = 0; r < TG; ++r) {
-                                if (r < nr) {
-                                    const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
-                                    if (lane == r) yv = sum * gsc;
-                                }
-                            }
-                            if (lane < nr) a.ws.Y[(size_t)(sd.row0 + r0 + lane) * d + c0 + q] = yv;
-                        }
-                    }
+                    float *yg = a.ws.Y + (size_t)(sd.row0 + r0) * d + c0;
+                    if (nr == 1)
+                        dn_group<1, FP4>(a, st, hg, 1, yg, gsc);
+                    else if (nr == 2)
+                        dn_group<(TG < 2 ? TG : 2), FP4>(a, st, hg, nr, yg, gsc);
+                    else if (nr <= 4)
+                        dn_group<(TG < 4 ? TG : 4), FP4>(a, st, hg, nr, yg, gsc);
+                    else
+                        dn_group<TG, FP4>(a, st, hg, nr, yg, gsc);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[slot]);
