@@ -89,6 +89,33 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
     return units_per_rank * world / t, t
 
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) per launch of the
+# dominant kernel, from one ncu capture: a 32-expert layer of the same kernel
+# (T=1 streams the same 8 experts), plus the 256-expert router's extra 1.84 MB.
+# Valid only for the kernel source it was taken on: the sha256 of the kernel's
+# source files must match, else the bench reports traffic as null.
+TRAFFIC = {
+    "decode_t1": {"bytes": 304.2e6 + 3.3e6,
+                  "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cu",
+                              "top_moe_expert_router_gb300/csrc/common.cuh"),
+                  "sha256": ("67395a8de9766f652ece05ceb28a5624dbff6347a879bcdb34345b8bffd3e044",
+                             "288137038e4343fe5f67a73751bf0be0bc9b7ff45faf4355d4583f8520766936")},
+}
+
+
+def measured_traffic(workload: str):
+    """Per-launch DRAM bytes of the captured kernel, or None if it changed since."""
+    import hashlib
+    t = TRAFFIC.get(workload)
+    if t is None:
+        return None
+    for src, want in zip(t["sources"], t["sha256"]):
+        with open(os.path.join(ROOT, src), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != want:
+                return None
+    return t["bytes"]
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -315,7 +342,9 @@ def run_ours(args):
         ly_ms = prof[:, 0].astype(np.float64)
         ly_gbs = float(layer_bytes.mean() / (ly_ms.mean() / 1e3) / 1e9)
         roofline = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": ly_gbs, "peak": hbm,
-                    "unit": "GB/s", "frac": ly_gbs / hbm, "traffic": None, "peak_source": peak_src,
+                    "unit": "GB/s", "frac": ly_gbs / hbm,
+                    "traffic": measured_traffic(args.workload) if not args.experts else None,
+                    "peak_source": peak_src,
                     "bytes_per_launch": float(layer_bytes.mean()), "ms_per_launch": float(ly_ms.mean())}
         kernel_ms = {"layer": float(ly_ms.mean())}
     elif prof.shape[1] == 4:
