@@ -42,9 +42,21 @@ struct Control {
     CtrLine cb_rows[32];     // fused decode kernel: expert rows done per 256-column block of Y
 };
 
+// Tokens per chunk of the large-batch routing (one 32-bit bitmap word per expert).
+constexpr int kRouteChunk = 32;
+
+// The large-batch router GEMM splits K (= d) in up to kRouterSplit parts, each
+// written to its own slice of the logits region; the top-k sums the parts in
+// order. d is a multiple of 64 (the GEMM's K block).
+constexpr int kRouterSplit = 4;
+inline int router_ksplit(int d) {
+    const int kb = d / 64;
+    return kb % kRouterSplit == 0 ? kRouterSplit : (kb % 2 == 0 ? 2 : 1);
+}
+
 struct Workspace {
     Control *ctrl;
-    float *logits;      // [max_T, E]
+    float *logits;      // [kRouterSplit][max_T, E] (decode: the first slice)
     int32_t *ids;       // [max_T, k]
     float *w;           // [max_T, k]
     int32_t *counts;    // [E]
@@ -58,8 +70,8 @@ struct Workspace {
     float *h;           // [max_T*k, I] fp32 (decode) / bf16 (prefill)
     float *Y;           // [max_T*k, d] fp32 expert outputs
     uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill)
-    int32_t *chunk_base;  // [ceil(max_T/256), E] per-chunk counts, then each chunk's first row per expert
-    uint32_t *chunk_bm;   // [ceil(max_T/256), E, 8] token bitmaps of each 256-token chunk
+    int32_t *chunk_base;  // [ceil(max_T/kRouteChunk), E] per-chunk counts, then each chunk's first row per expert
+    uint32_t *chunk_bm;   // [ceil(max_T/kRouteChunk), E] token bitmaps of each kRouteChunk-token chunk
     size_t bytes;
 };
 
@@ -76,7 +88,7 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     };
     size_t Tk = (size_t)max_T * k;
     ws.ctrl = (Control *)take(sizeof(Control));
-    ws.logits = (float *)take(sizeof(float) * (size_t)max_T * E);
+    ws.logits = (float *)take(sizeof(float) * (size_t)kRouterSplit * max_T * E);
     ws.ids = (int32_t *)take(sizeof(int32_t) * Tk);
     ws.w = (float *)take(sizeof(float) * Tk);
     ws.counts = (int32_t *)take(sizeof(int32_t) * E);
@@ -90,9 +102,9 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     ws.h = (float *)take(sizeof(float) * Tk * I);
     ws.Y = (float *)take(sizeof(float) * Tk * d);
     ws.xperm = (uint16_t *)take(sizeof(uint16_t) * Tk * d);
-    const size_t nchunks = ((size_t)max_T + 255) / 256;
+    const size_t nchunks = ((size_t)max_T + kRouteChunk - 1) / kRouteChunk;
     ws.chunk_base = (int32_t *)take(sizeof(int32_t) * nchunks * E);
-    ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E * 8);
+    ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E);
     ws.bytes = off;
     return ws;
 }
@@ -110,6 +122,75 @@ __device__ __forceinline__ unsigned long long global_ns() {
     unsigned long long t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
+}
+
+// Order-preserving map of a float to an unsigned key (larger float, larger
+// key; -0 is taken as +0 so that equal values tie). Key 0 lies below every
+// float and marks "no candidate".
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
+    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+__device__ __forceinline__ float key_value(uint32_t key) {
+    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
+}
+
+// Top-k (k <= 8, E <= 256) of one token's logits by one warp: ids by
+// descending logit, ties to the lower id; weights exp(l - l_max) / sum over
+// the kept, summed in pick order. Lane l holds experts l, l + 32, ...; each
+// pick is a warp-wide max of the lanes' best keys and a warp-wide min of the
+// ids that reach it. bypass_l1: read the logits through L2 only (they were
+// written by other CTAs of the same launch). nsplit > 1: the logit is the sum,
+// in order, of nsplit parts split_stride floats apart.
+__device__ __forceinline__ void topk_warp(const float *logits_row, int E, int k, int32_t *ids_out, float *w_out,
+                                          bool bypass_l1, int nsplit = 1, size_t split_stride = 0) {
+    const int lane = threadIdx.x & 31;
+    uint32_t key[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = lane + 32 * i;
+        float l = 0.f;
+        if (e < E) {
+            // the logit's parts over K, added in order
+            l = bypass_l1 ? __ldcg(logits_row + e) : logits_row[e];
+            for (int s = 1; s < nsplit; ++s)
+                l += bypass_l1 ? __ldcg(logits_row + s * split_stride + e) : logits_row[s * split_stride + e];
+        }
+        key[i] = e < E ? order_key(l) : 0u;
+    }
+    uint32_t my_key = 0u;
+    int my_id = 0;
+    for (int j = 0; j < k; ++j) {
+        // this lane's best: largest key, the lowest i (= lowest id) among equals
+        uint32_t bk = key[0];
+        int bi = 0;
+#pragma unroll
+        for (int i = 1; i < 8; ++i)
+            if (key[i] > bk) {
+                bk = key[i];
+                bi = i;
+            }
+        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
+        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
+        if ((int)(win & 31u) == lane) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (i == (int)(win >> 5)) key[i] = 0u;
+        }
+        if (lane == j) {
+            my_key = m;
+            my_id = (int)win;
+        }
+    }
+    const float lmax = __shfl_sync(0xFFFFFFFFu, key_value(my_key), 0);
+    const float ex = lane < k ? expf(key_value(my_key) - lmax) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) {
+        ids_out[lane] = my_id;
+        w_out[lane] = ex / sum;
+    }
 }
 
 // Release/acquire fence at GPU scope: with a relaxed atomic it orders this

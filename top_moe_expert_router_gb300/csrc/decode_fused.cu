@@ -220,64 +220,6 @@ __device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
     for (int r = 0; r < TM; ++r) s.tok[r] = r < s.n_e ? R.perm[s.row0 + r] : 0;
 }
 
-// Order-preserving map of a float to an unsigned key (larger float, larger
-// key; -0 is taken as +0 so that equal values tie). Key 0 lies below every
-// float and marks "no candidate".
-__device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t u = __float_as_uint(f == 0.f ? 0.f : f);
-    return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
-
-__device__ __forceinline__ float key_value(uint32_t key) {
-    return __uint_as_float((key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key);
-}
-
-// top-k of one token by one warp, weights exp(l - lmax) / sum over the kept.
-// Lane l holds experts l, l + 32, ...; each pick is one warp-wide max of the
-// lanes' best keys and one warp-wide min of the ids that reach it (ties go to
-// the lower id).
-__device__ void topk_to_smem(const float *logits_row, int E, int k, int32_t *ids, float *w) {
-    const int lane = threadIdx.x & 31;
-    uint32_t key[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int e = lane + 32 * i;
-        key[i] = e < E ? order_key(__ldcg(logits_row + e)) : 0u;
-    }
-    uint32_t my_key = 0u;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-        // this lane's best: largest key, the lowest i (= lowest id) among equals
-        uint32_t bk = key[0];
-        int bi = 0;
-#pragma unroll
-        for (int i = 1; i < 8; ++i)
-            if (key[i] > bk) {
-                bk = key[i];
-                bi = i;
-            }
-        const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, bk);
-        const uint32_t win = __reduce_min_sync(0xFFFFFFFFu, bk == m ? (uint32_t)(lane + 32 * bi) : 0xFFFFFFFFu);
-        if ((int)(win & 31u) == lane) {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                if (i == (int)(win >> 5)) key[i] = 0u;
-        }
-        if (lane == j) {
-            my_key = m;
-            my_id = (int)win;
-        }
-    }
-    const float lmax = __shfl_sync(0xFFFFFFFFu, key_value(my_key), 0);
-    const float ex = lane < k ? expf(key_value(my_key) - lmax) : 0.f;
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);  // picks in order, as a running sum
-    if (lane < k) {
-        ids[lane] = my_id;
-        w[lane] = ex / sum;
-    }
-}
-
 // exclusive scan of a[0..n) (n <= 256) by one warp; returns the total
 __device__ int warp_scan256(const int32_t *a, int32_t *out, int n) {
     const int lane = threadIdx.x & 31;
@@ -389,6 +331,10 @@ __device__ __forceinline__ void gu_stage(const Args &a, const unsigned char *st,
             // tokens in shared memory as fp16(x / max|x|): the 16 products
             // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
             // pairs, then scaled by the block scale and max|x| in fp32
+            float xsc[NE];  // per-token max|x|
+#pragma unroll
+            for (int r = 0; r < NE; ++r) xsc[r] = (NE <= 2 || r < seg.n_e) ? xscale[seg.tok[r]] : 0.f;
+#pragma unroll 2
             for (int bb = lane; bb < d / 16; bb += 32) {
                 const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
                 const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
@@ -410,17 +356,21 @@ __device__ __forceinline__ void gu_stage(const Args &a, const unsigned char *st,
                         const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2;
                         const uint4 xa = xp[0], xb = xp[1];
                         const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                        __half2 pg = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
-                        __half2 pu = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+                        // two chains per matrix (even / odd pairs), joined at the end
+                        __half2 pg0 = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+                        __half2 pu0 = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
+                        __half2 pg1 = __hmul2(gh[1], *reinterpret_cast<const __half2 *>(&xw[1]));
+                        __half2 pu1 = __hmul2(uh[1], *reinterpret_cast<const __half2 *>(&xw[1]));
 #pragma unroll
-                        for (int q = 1; q < 8; ++q) {
-                            pg = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg);
-                            pu = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu);
+                        for (int q = 2; q < 8; q += 2) {
+                            pg0 = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg0);
+                            pu0 = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu0);
+                            pg1 = __hfma2(gh[q + 1], *reinterpret_cast<const __half2 *>(&xw[q + 1]), pg1);
+                            pu1 = __hfma2(uh[q + 1], *reinterpret_cast<const __half2 *>(&xw[q + 1]), pu1);
                         }
-                        const float2 fg = __half22float2(pg), fu = __half22float2(pu);
-                        const float xsc = xscale[seg.tok[r]];
-                        ag[r].x = fmaf(fg.x + fg.y, sgb * xsc, ag[r].x);
-                        au[r].x = fmaf(fu.x + fu.y, sub * xsc, au[r].x);
+                        const float2 fg = __half22float2(__hadd2(pg0, pg1)), fu = __half22float2(__hadd2(pu0, pu1));
+                        ag[r].x = fmaf(fg.x + fg.y, sgb * xsc[r], ag[r].x);
+                        au[r].x = fmaf(fu.x + fu.y, sub * xsc[r], au[r].x);
                     }
                 }
             }
@@ -538,6 +488,16 @@ __device__ __forceinline__ void dn_group(const Args &a, const unsigned char *st,
     } else {
         const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
         for (int bb = lane; bb < I / 16; bb += 32) {
+            // the block's 16 h values of each token, loaded once for all rows
+            float4 hv[NG][4];
+#pragma unroll
+            for (int r = 0; r < NG; ++r) {
+                if (NG <= 2 || r < nr) {
+                    const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
+#pragma unroll
+                    for (int h4 = 0; h4 < 4; ++h4) hv[r][h4] = __ldcg(hp + h4);
+                }
+            }
 #pragma unroll
             for (int q = 0; q < kDnRows; ++q) {
                 float2 wf[8];
@@ -546,13 +506,11 @@ __device__ __forceinline__ void dn_group(const Args &a, const unsigned char *st,
 #pragma unroll
                 for (int r = 0; r < NG; ++r) {
                     if (NG <= 2 || r < nr) {
-                        const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
                         float2 p = make_float2(0.f, 0.f);
 #pragma unroll
                         for (int h4 = 0; h4 < 4; ++h4) {
-                            const float4 hv = __ldcg(hp + h4);
-                            p = ffma2(wf[2 * h4], make_float2(hv.x, hv.y), p);
-                            p = ffma2(wf[2 * h4 + 1], make_float2(hv.z, hv.w), p);
+                            p = ffma2(wf[2 * h4], make_float2(hv[r][h4].x, hv[r][h4].y), p);
+                            p = ffma2(wf[2 * h4 + 1], make_float2(hv[r][h4].z, hv[r][h4].w), p);
                         }
                         acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
                     }
@@ -734,7 +692,7 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
 
     // ---- 2. routing, computed by every CTA in shared memory ----
     for (int t = warp; t < T; t += kConsumers + 1)
-        topk_to_smem(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k);
+        topk_warp(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k, true);
     if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
     if (warp == 0) {
         // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
@@ -979,6 +937,53 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
                 if (lane == 0) mbar_arrive(&empty[slot]);
                 store_four_rows(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y, acc[3].x + acc[3].y,
                                 a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
+            } else if (FP4 && sd.n_e == 1 && I / 16 <= 32 * (kHC / 2)) {
+                // NVFP4, one token: lane block j (16 elements of h) held in
+                // hc0[2j], hc0[2j+1], hc1[2j], hc1[2j+1] across the expert's stages
+                if (hc_u != sd.u) {
+#pragma unroll
+                    for (int j = 0; j < kHC / 2; ++j) {
+                        const int bb = lane + 32 * j;
+                        if (bb < I / 16) {
+                            const float4 *hp = reinterpret_cast<const float4 *>(hrow + bb * 16);
+                            hc0[2 * j] = __ldcg(hp);
+                            hc0[2 * j + 1] = __ldcg(hp + 1);
+                            hc1[2 * j] = __ldcg(hp + 2);
+                            hc1[2 * j + 1] = __ldcg(hp + 3);
+                        }
+                    }
+                    hc_u = sd.u;
+                }
+                const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
+                float acc[kDnRows];
+#pragma unroll
+                for (int q = 0; q < kDnRows; ++q) acc[q] = 0.f;
+#pragma unroll
+                for (int j = 0; j < kHC / 2; ++j) {
+                    const int bb = lane + 32 * j;
+                    if (bb < I / 16) {
+                        const float4 h0 = hc0[2 * j], h1 = hc0[2 * j + 1], h2 = hc1[2 * j], h3 = hc1[2 * j + 1];
+#pragma unroll
+                        for (int q = 0; q < kDnRows; ++q) {
+                            float2 wf[8];
+                            fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
+                            const float sc = e4m3f(sb[q * (I / 16) + bb]);
+                            float2 p = make_float2(0.f, 0.f), p1 = make_float2(0.f, 0.f);
+                            p = ffma2(wf[0], make_float2(h0.x, h0.y), p);
+                            p1 = ffma2(wf[1], make_float2(h0.z, h0.w), p1);
+                            p = ffma2(wf[2], make_float2(h1.x, h1.y), p);
+                            p1 = ffma2(wf[3], make_float2(h1.z, h1.w), p1);
+                            p = ffma2(wf[4], make_float2(h2.x, h2.y), p);
+                            p1 = ffma2(wf[5], make_float2(h2.z, h2.w), p1);
+                            p = ffma2(wf[6], make_float2(h3.x, h3.y), p);
+                            p1 = ffma2(wf[7], make_float2(h3.z, h3.w), p1);
+                            acc[q] = fmaf((p.x + p1.x) + (p.y + p1.y), sc, acc[q]);
+                        }
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[slot]);
+                store_four_rows(acc[0], acc[1], acc[2], acc[3], a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
             } else {
                 // the expert's tokens in groups of up to TG (bounded registers)
                 constexpr int TG = TM < 4 ? TM : 4;

@@ -51,6 +51,8 @@ struct GemmParams {
     int n_valid;              // columns < n_valid are stored (router: E)
     const float *bias;
     uint32_t *err;
+    int ksplit;               // single group only: K split in ksplit parts, part s written at out_f32 + s * split_stride
+    size_t split_stride;
 };
 
 // ---------------------------------------------------------------------------
@@ -125,11 +127,11 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN 
 // tile scheduling
 // ---------------------------------------------------------------------------
 struct TileInfo {
-    int g, m, n, row0, rows;
+    int g, m, n, row0, rows, ks;
 };
 
 __device__ __forceinline__ int total_tiles(const GemmParams &p) {
-    if (!p.tile_off) return ((p.n_rows + BM - 1) / BM) * p.nt;
+    if (!p.tile_off) return ((p.n_rows + BM - 1) / BM) * p.nt * p.ksplit;
     return p.tile_off[p.groups] * p.nt;
 }
 
@@ -139,7 +141,8 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile) {
         const int mt = (p.n_rows + BM - 1) / BM;
         ti.g = 0;
         ti.m = tile % mt;
-        ti.n = tile / mt;
+        ti.n = (tile / mt) % p.nt;
+        ti.ks = tile / (mt * p.nt);
         ti.row0 = 0;
         ti.rows = p.n_rows;
         return ti;
@@ -156,6 +159,7 @@ __device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile) {
     const int mt = p.tile_off[lo + 1] - p.tile_off[lo];
     const int local = tile - p.tile_off[lo] * p.nt;
     ti.g = lo;
+    ti.ks = 0;
     ti.m = local % mt;
     ti.n = local / mt;
     ti.row0 = p.row_off[lo];
@@ -202,7 +206,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
     const int ntiles = total_tiles(p);
-    const int kblocks = p.K / BK;
+    const int kblocks = p.K / BK / p.ksplit;  // k-blocks of one tile
 
     if (warp == 0) {
         // ------------------------------- TMA producer -------------------------------
@@ -213,7 +217,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const TileInfo ti = tile_info(p, tile);
                 const int arow = ti.row0 + ti.m * BM;
                 const int brow = ti.g * p.b_rows_per_group + ti.n * (SPLIT_B ? BN / 2 : BN);
-                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int kb0 = ti.ks * kblocks;
+                for (int kb = kb0; kb < kb0 + kblocks; ++kb, ++it) {
                     const int slot = it % kGemmStages;
                     if (!mbar_wait_or_abort(&empty[slot], ((it / kGemmStages) & 1) ^ 1, err, abort_flag)) {
                         ok = false;
@@ -306,12 +311,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_ld_wait();
                     const int col0 = ti.n * BN + j0;
                     if (valid) {
-                        float *dst = p.out_f32 + orow * p.ld + col0;
+                        float *dst = p.out_f32 + (size_t)ti.ks * p.split_stride + orow * p.ld + col0;
                         if (EPI == EPI_LOGITS) {
+                            const bool add_bias = p.bias && ti.ks == 0;  // once, with the first part of K
 #pragma unroll
                             for (int i = 0; i < 16; ++i)
                                 if (col0 + i < p.n_valid)
-                                    dst[i] = __uint_as_float(v[i]) + (p.bias ? p.bias[col0 + i] : 0.f);
+                                    dst[i] = __uint_as_float(v[i]) + (add_bias ? p.bias[col0 + i] : 0.f);
                         } else {
 #pragma unroll
                             for (int i = 0; i < 16; i += 4)
@@ -394,7 +400,11 @@ cudaError_t launch_router_gemm(const LayerDev &L, const Workspace &ws, const uin
     p.n_valid = L.E;
     p.bias = L.bias;
     p.err = &ws.ctrl->err;
-    int tiles = ((T + BM - 1) / BM) * p.nt;
+    // K in kRouterSplit parts (partial logits summed in order by the top-k):
+    // T = 4096 has only 32 row tiles, too few for the SMs
+    p.ksplit = router_ksplit(L.d);
+    p.split_stride = (size_t)L.max_T * L.E;
+    int tiles = ((T + BM - 1) / BM) * p.nt * p.ksplit;
     int grid = tiles < L.num_sms ? tiles : L.num_sms;
     return launch_gemm<EPI_LOGITS, false>(ta, tb, tb, p, grid, st);
 }
@@ -411,6 +421,7 @@ cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const
         !make_tmap_bf16(&td, L.wd, (uint64_t)L.E * L.d, (uint64_t)L.I, BN))
         return cudaErrorInvalidValue;
     GemmParams p{};
+    p.ksplit = 1;
     p.tile_off = ws.tile_off;
     p.row_off = ws.offsets;
     p.groups = L.E;

@@ -14,60 +14,6 @@
 namespace moe {
 
 // ---------------------------------------------------------------------------
-// top-k of one token's logits by one warp
-// ---------------------------------------------------------------------------
-// Selection on logits is the same as selection on softmax probabilities
-// (exp is increasing); ties go to the lower expert id. The kept weights are
-// p_j / sum(p_sel) = exp(l_j - l_max) / sum exp(l_sel - l_max) in fp32.
-__device__ void topk_warp(const float *logits_row, int E, int k, int32_t *ids_out, float *w_out, bool bypass_l1) {
-    const int lane = threadIdx.x & 31;
-    float v[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        int e = lane + 32 * i;
-        v[i] = (e < E) ? (bypass_l1 ? __ldcg(logits_row + e) : logits_row[e]) : -INFINITY;
-    }
-    uint32_t taken = 0;
-    float lmax = 0.f, sum = 0.f;
-    float my_val = 0.f;
-    int my_id = 0;
-    for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int bi = 0x7FFFFFFF;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            int e = lane + 32 * i;
-            bool ok = (e < E) && !((taken >> i) & 1u);
-            if (ok && (v[i] > bv || (v[i] == bv && e < bi))) {
-                bv = v[i];
-                bi = e;
-            }
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            float ov = __shfl_xor_sync(0xFFFFFFFFu, bv, o);
-            int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ov > bv || (ov == bv && oi < bi)) {
-                bv = ov;
-                bi = oi;
-            }
-        }
-        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-        if (j == 0) lmax = bv;
-        float ex = expf(bv - lmax);
-        sum += ex;
-        if (lane == j) {
-            my_val = ex;
-            my_id = bi;
-        }
-    }
-    if (lane < k) {
-        ids_out[lane] = my_id;
-        w_out[lane] = my_val / sum;
-    }
-}
-
-// ---------------------------------------------------------------------------
 // permutation by one CTA
 // ---------------------------------------------------------------------------
 // Shared memory needed: (4 * (E + 1) * 4) + E * words * 4 bytes, words = chunk / 32.
@@ -269,35 +215,34 @@ cudaError_t launch_route_small(const LayerDev &L, const Workspace &ws, const uin
 //   route_scatter_kernel: one CTA per chunk places every (token, slot) pair at
 //     chunk_base[chunk][e] + (tokens of e earlier in the chunk).
 // ---------------------------------------------------------------------------
-constexpr int kChunk = 256;              // tokens per chunk
-constexpr int kChunkWords = kChunk / 32;
+constexpr int kChunk = kRouteChunk;      // tokens per chunk: one bitmap word per expert
+static_assert(kChunk == 32, "one 32-bit bitmap word per expert and chunk");
 
-__global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, Workspace ws) {
-    __shared__ uint32_t bm[256 * kChunkWords];
+__global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, int nsplit, size_t split_stride,
+                                                          Workspace ws) {
+    __shared__ uint32_t bm[256];
     __shared__ int32_t s_cnt[257], s_off[257], s_flag[257], s_idx[257];
     __shared__ int s_last;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int c = blockIdx.x, t0 = c * kChunk;
     const int nt = min(kChunk, T - t0);
-    for (int i = tid; i < E * kChunkWords; i += 256) bm[i] = 0u;
+    for (int i = tid; i < E; i += 256) bm[i] = 0u;
     __syncthreads();
     for (int tl = warp; tl < nt; tl += 8) {
         const int t = t0 + tl;
-        topk_warp(ws.logits + (size_t)t * E, E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false);
+        topk_warp(ws.logits + (size_t)t * E, E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false, nsplit,
+                  split_stride);
         __syncwarp();
         if (lane < k) {
             const int e = ws.ids[(size_t)t * k + lane];
-            atomicOr(&bm[e * kChunkWords + (tl >> 5)], 1u << (tl & 31));
+            atomicOr(&bm[e], 1u << tl);
         }
     }
     __syncthreads();
-    uint32_t *gbm = ws.chunk_bm + (size_t)c * E * kChunkWords;
-    for (int i = tid; i < E * kChunkWords; i += 256) gbm[i] = bm[i];
+    uint32_t *gbm = ws.chunk_bm + (size_t)c * E;
     for (int e = tid; e < E; e += 256) {
-        int n = 0;
-#pragma unroll
-        for (int w8 = 0; w8 < kChunkWords; ++w8) n += __popc(bm[e * kChunkWords + w8]);
-        ws.chunk_base[(size_t)c * E + e] = n;
+        gbm[e] = bm[e];
+        ws.chunk_base[(size_t)c * E + e] = __popc(bm[e]);
     }
     // last-CTA hand-off: the CTA that completes the count scans for everyone
     __threadfence();
@@ -309,6 +254,7 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, W
     const int nch = gridDim.x;
     for (int e = tid; e < E; e += 256) {
         int n = 0;
+#pragma unroll 8
         for (int cc = 0; cc < nch; ++cc) n += __ldcg(ws.chunk_base + (size_t)cc * E + e);
         s_cnt[e] = n;
         s_flag[e] = n > 0 ? 1 : 0;
@@ -350,7 +296,7 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, W
 __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int k, int E, Workspace ws) {
     const int c = blockIdx.x, t0 = c * kChunk;
     const int nt = min(kChunk, T - t0);
-    const uint32_t *gbm = ws.chunk_bm + (size_t)c * E * kChunkWords;
+    const uint32_t *gbm = ws.chunk_bm + (size_t)c * E;
     for (int p = threadIdx.x; p < nt * k; p += 256) {
         const int tl = p / k;
         const int t = t0 + tl;
@@ -359,10 +305,7 @@ __global__ void __launch_bounds__(256) route_scatter_kernel(int T, int k, int E,
             atomicOr(&ws.ctrl->err, ERRBIT_RANGE);
             continue;
         }
-        const uint32_t *b = gbm + e * kChunkWords;
-        int rank = 0;
-        for (int w8 = 0; w8 < (tl >> 5); ++w8) rank += __popc(b[w8]);
-        rank += __popc(b[tl >> 5] & ((1u << (tl & 31)) - 1u));
+        const int rank = __popc(gbm[e] & ((1u << tl) - 1u));
         const int row = ws.chunk_base[(size_t)c * E + e] + rank;
         ws.perm[row] = t;
         ws.pos[(size_t)t0 * k + p] = row;
@@ -374,7 +317,7 @@ cudaError_t launch_route_large(const LayerDev &L, const Workspace &ws, const uin
     cudaError_t e = launch_router_gemm(L, ws, x, T, st);
     if (e != cudaSuccess) return e;
     const int nch = (T + kChunk - 1) / kChunk;
-    route_chunk_kernel<<<nch, 256, 0, st>>>(T, L.k, L.E, ws);
+    route_chunk_kernel<<<nch, 256, 0, st>>>(T, L.k, L.E, router_ksplit(L.d), (size_t)L.max_T * L.E, ws);
     route_scatter_kernel<<<nch, 256, 0, st>>>(T, L.k, L.E, ws);
     *launches += 3;
     return cudaGetLastError();
