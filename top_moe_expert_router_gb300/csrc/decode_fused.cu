@@ -36,9 +36,17 @@ namespace moe {
 
 namespace fused {
 
-constexpr int kConsumers = 7;                 // consumer warps at most (8 warps in all)
-constexpr int kThreads = 32 * (kConsumers + 1);
-constexpr int kProducerWarp = kConsumers;
+// Warps per CTA: 7 consumers and the producer. Registers are handed out per
+// group of four warps, so a CTA of 4n warps wastes none; a 9-warp CTA would be
+// charged for 12 (capping a thread at 168 registers). (12-warp NVFP4 CTAs
+// were measured slower: fewer ring slots per consumer and fewer producer lanes.)
+template <int TM, bool FP4>
+struct Warps {
+    static constexpr int kWarps = 8;
+    static constexpr int kThreads = 32 * kWarps;
+    static constexpr int kConsumers = kWarps - 1;   // consumer warps at most
+    static constexpr int kProducerWarp = kWarps - 1;
+};
 constexpr int kDnRows = 4;                    // down rows per stage
 constexpr int kMaxSlots = 32;
 constexpr int kSmemBudget = 227 * 1024;
@@ -542,7 +550,10 @@ __device__ __forceinline__ void dn_group(const Args &a, const unsigned char *st,
 // the kernel
 // ---------------------------------------------------------------------------
 template <int TM, bool FP4>
-__global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
+__global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kernel(Args a) {
+    constexpr int kThreads = Warps<TM, FP4>::kThreads;
+    constexpr int kConsumers = Warps<TM, FP4>::kConsumers;
+    constexpr int kProducerWarp = Warps<TM, FP4>::kProducerWarp;
     extern __shared__ __align__(128) unsigned char smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int d = a.d, I = a.I, E = a.E, k = a.k, T = a.T, NS = a.nslots, C = a.ncons;
@@ -694,7 +705,42 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     for (int t = warp; t < T; t += kConsumers + 1)
         topk_warp(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k, true);
     if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
-    if (warp == 0) {
+    if (warp == 0 && T == 1) {
+        // one token: its k distinct experts, ascending, are the k rows
+        __syncwarp();
+        const int my = lane < k ? R.ids[lane] : 0x7FFFFFFF;
+        int rank = 0;
+        int cnt_i[8], off_i[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) cnt_i[i] = off_i[i] = 0;
+        for (int q = 0; q < k; ++q) {
+            const int o = __shfl_sync(0xFFFFFFFFu, my, q);
+            rank += o < my;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                cnt_i[i] += o == e;
+                off_i[i] += o < e;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            if (e < E) {
+                R.cnt[e] = cnt_i[i];
+                R.off[e] = off_i[i];
+            }
+        }
+        if (lane < k) {
+            R.uniq[rank] = my;
+            R.perm[rank] = 0;
+            R.pos[lane] = rank;
+        }
+        if (lane == 0) {
+            R.off[E] = k;
+            *R.n_uniq = k;
+        }
+    } else if (warp == 0) {
         // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
         // tokens ascending within an expert
         __syncwarp();
@@ -1079,10 +1125,10 @@ __global__ void __launch_bounds__(kThreads, 1) decode_layer_kernel(Args a) {
     }
 }
 
-template <bool FP4>
+template <int TM, bool FP4>
 static int pick(int fit, int &ncons) {
     if (fit > kMaxSlots) fit = kMaxSlots;
-    for (int c = kConsumers; c >= 1; --c)
+    for (int c = Warps<TM, FP4>::kConsumers; c >= 1; --c)
         if (fit / c >= 2) {
             ncons = c;
             return (fit / c) * c;
@@ -1131,7 +1177,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     const size_t xb2 = a.x_in_smem ? xb : 0;
     if (fixed + xb2 + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
     const int fit = (int)((kSmemBudget - fixed - xb2) / a.slot_bytes);
-    a.nslots = pick<FP4>(fit, a.ncons);
+    a.nslots = pick<TM, FP4>(fit, a.ncons);
     a.x_router_ring = !a.x_in_smem && (size_t)a.nslots * a.slot_bytes >= (size_t)T * L.d * 2 ? 1 : 0;
     a.nprod = a.nslots % 4 == 0 ? 4 : (a.nslots % 2 == 0 ? 2 : 1);
     const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
@@ -1144,7 +1190,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(Warps<TM, FP4>::kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attrs[1];
