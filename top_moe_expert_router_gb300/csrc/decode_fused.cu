@@ -158,6 +158,50 @@ __device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, in
     return p;
 }
 
+// Cost of one stage of an expert with n tokens, in arbitrary units: every
+// stage streams the same bytes, the arithmetic grows with the tokens.
+__device__ __forceinline__ int stage_weight(int n) { return 2 + n; }
+
+// Index, within a segment of experts [u_lo, u_hi) holding `per` stages each,
+// where CTA bb's share starts when the segment is cut into G parts of equal
+// total weight (bb = G gives the segment's end). cw: exclusive prefix over
+// experts of one stage's weight.
+__device__ __forceinline__ int weighted_start(const int32_t *cw, int u_lo, int u_hi, int per, int bb, int G) {
+    if (u_hi <= u_lo) return 0;
+    if (bb >= G) return (u_hi - u_lo) * per;
+    const long long base = cw[u_lo];
+    const long long t = (long long)(cw[u_hi] - base) * per * bb / G;
+    int lo = u_lo, hi = u_hi;  // the expert holding weight position t
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if ((long long)(cw[mid] - base) * per <= t)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const long long w = cw[lo + 1] - cw[lo];
+    const long long j = (t - (long long)(cw[lo] - base) * per + w - 1) / w;
+    return (lo - u_lo) * per + (int)(j < per ? j : per);
+}
+
+// make_plan with the segments cut by weight instead of by stage count.
+__device__ __forceinline__ Plan make_plan_weighted(const int32_t *cw, int U, int I, int units_per_expert, int b,
+                                                   int G) {
+    Plan p;
+    const int U1 = (U + 1) / 2;
+    p.a0 = weighted_start(cw, 0, U1, I, b, G);
+    p.nA = weighted_start(cw, 0, U1, I, b + 1, G) - p.a0;
+    p.b0 = weighted_start(cw, U1, U, I, b, G);
+    p.nB = weighted_start(cw, U1, U, I, b + 1, G) - p.b0;
+    p.c0 = weighted_start(cw, 0, U1, units_per_expert, b, G);
+    p.nC = weighted_start(cw, 0, U1, units_per_expert, b + 1, G) - p.c0;
+    p.d0 = weighted_start(cw, U1, U, units_per_expert, b, G);
+    p.nD = weighted_start(cw, U1, U, units_per_expert, b + 1, G) - p.d0;
+    p.offB = U1 * I;
+    p.offD = U1 * units_per_expert;
+    return p;
+}
+
 // Publish a warp's count of finished h rows (all lanes' h stores first).
 __device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
     fence_acq_rel_gpu();
@@ -806,7 +850,23 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     // segment earlier, so the stream does not stop between the two
     // projections. A wait only ever sits at a down stage, and every stage that
     // feeds the counts comes earlier in every CTA's order, so the waits end.
-    const Plan pl = make_plan(n_uniq, I, d / kDnRows, b, G);
+    // One token: every expert costs the same, equal shares. More: experts
+    // with more tokens cost more per stage; the shares are cut by weight.
+    Plan pl;
+    if (T == 1) {
+        pl = make_plan(n_uniq, I, d / kDnRows, b, G);
+    } else {
+        int32_t *cw = R.scan;  // free after the permutation
+        int32_t *wt = reinterpret_cast<int32_t *>(R.bm);
+        if (warp == 0) {
+            for (int u = lane; u < n_uniq; u += 32) wt[u] = stage_weight(min(R.cnt[R.uniq[u]], TM));
+            __syncwarp();
+            const int total = warp_scan256(wt, cw, n_uniq);
+            if (lane == 0) cw[n_uniq] = total;
+        }
+        __syncthreads();
+        pl = make_plan_weighted(cw, n_uniq, I, d / kDnRows, b, G);
+    }
     const int n_gu = pl.nA + pl.nB;
     const int n_st = n_gu + pl.nC + pl.nD;
     const int U1 = (n_uniq + 1) / 2;
