@@ -160,7 +160,7 @@ __device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, in
 
 // Cost of one stage of an expert with n tokens, in arbitrary units: every
 // stage streams the same bytes, the arithmetic grows with the tokens.
-__device__ __forceinline__ int stage_weight(int n) { return 1 + 2 * n; }
+__device__ __forceinline__ int stage_weight(int n) { return n; }
 
 // Index, within a segment of experts [u_lo, u_hi) holding `per` stages each,
 // where CTA bb's share starts when the segment is cut into G parts of equal
