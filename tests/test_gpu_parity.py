@@ -82,7 +82,7 @@ def _full_gpu_layer(moe, dev, max_tokens, bias):
 # tiny layer: every token, several batch sizes, ragged chunks
 # --------------------------------------------------------------------------
 
-@pytest.mark.parametrize("T", [8, 1, 3, 16, 17, 40])
+@pytest.mark.parametrize("T", [8, 1, 2, 3, 5, 16, 17, 40])
 def test_tiny_every_token(tiny, T):
     host, gl = tiny
     x = datagen.tokens(host.w, T, start_row=100 if T != 8 else 0)
@@ -176,6 +176,19 @@ def test_decode_full_size_every_token(gpu_lib, full_layer, T, start):
     gl = _full_gpu_layer(gpu_lib, dev, max_tokens=16, bias=False)
     x = datagen.tokens(D4096, T, start_row=start)
     st = _parity(gl, host.oracle(bias=False), x, 256, BF16_TOL)
+    assert st["err"] < 1e-2
+
+
+def test_decode_full_size_skewed_routing(gpu_lib, full_layer):
+    """16 tokens under the skewed router bias: a few experts take many of the
+    tokens, so the stage shares are cut by cost, not by count."""
+    host, dev = full_layer
+    gl = _full_gpu_layer(gpu_lib, dev, max_tokens=16, bias=True)
+    x = datagen.tokens(D4096, 16, start_row=300)
+    r = gl.route(to_dev_bf16(x))
+    counts = r["counts"].cpu().numpy()
+    assert counts.max() >= 3                       # multi-token experts present
+    st = _parity(gl, host.oracle(bias=True), x, 256, BF16_TOL)
     assert st["err"] < 1e-2
 
 
