@@ -128,7 +128,9 @@ moe_status moe_forward_host(moe_layer *layer, const void *x_host, void *out_host
 
 /* Expert outputs of the last forward on this layer, before the weighted sum:
  * Y [T*k, d] fp32, row pos[t, j] holding expert ids[t, j] applied to token t
- * (pos from moe_route on the same x). For parity checks of every slot. */
+ * (pos from moe_route on the same x). For parity checks of every slot. After
+ * a large-batch forward the outputs were kept in bf16 (the grouped GEMMs'
+ * output precision) and are widened to fp32 here. */
 moe_status moe_debug_expert_outputs(moe_layer *layer, float *Y, int T, void *stream);
 
 /* Row-wise RMSNorm without a learned scale: out = x / sqrt(mean(x^2) + eps),

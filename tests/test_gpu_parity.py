@@ -210,10 +210,16 @@ def test_prefill_full_size_routing_all_and_output_sample(gpu_lib, full_layer):
     assert 3.0 < counts.max() / counts.mean() < 5.0       # the skewed load the workload asks for
     sample = np.sort(np.random.default_rng(1).choice(T, 256, replace=False))
     gpu_ids = r["ids"].cpu().numpy()
-    ref = L.forward(x, tokens=sample, forced_ids=gpu_ids)
+    ref = L.forward(x, tokens=sample, forced_ids=gpu_ids, want_Y=True)
     ref_ids_own = ids[sample]
     assert (ref["ids"] == gpu_ids[sample]).all()
     near = gap[sample] <= 1e-3
     assert ((ref_ids_own == gpu_ids[sample]).all(1) | near).all()
     err = normwise_rel_err(datagen.bf16_to_f32(bf16_host(y))[sample], ref["y"])
     assert err.max() <= BF16_TOL
+    # every slot of the sample: the grouped GEMMs' expert outputs (kept in bf16)
+    Y = gl.expert_outputs(T)
+    pos = r["pos"].cpu().numpy()[sample]
+    Yg = Y[torch.from_numpy(pos.reshape(-1)).to(Y.device)].cpu().numpy().reshape(len(sample), 8, -1)
+    del Y
+    assert normwise_rel_err(Yg, ref["Y"]).max() <= BF16_TOL

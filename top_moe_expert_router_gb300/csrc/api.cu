@@ -14,6 +14,7 @@ struct moe_layer {
     moe::LayerDev L;
     moe::Workspace ws;
     int last_launches;
+    bool y_bf16 = false;  // the last forward left the expert outputs in bf16 over ws.xperm
     // profiling: events [forward][kernel boundary]
     std::vector<cudaEvent_t> prof_events;
     int prof_max = 0, prof_count = 0, prof_nk = 0;
@@ -89,8 +90,10 @@ moe_status forward_prefill(moe_layer *ly, const uint16_t *x, const uint16_t *res
     prof_mark(ly, 1, st);
     if (e == cudaSuccess) e = launch_prefill_experts(L, ly->ws, x, T, st, &launches);
     prof_mark(ly, 2, st);
-    if (e == cudaSuccess) e = launch_combine(L, ly->ws, res, out, T, st);
+    const bool y_bf16 = !L.expert_norm;  // the down GEMM's bf16 expert outputs
+    if (e == cudaSuccess) e = launch_combine(L, ly->ws, res, out, T, st, y_bf16);
     ++launches;
+    ly->y_bf16 = y_bf16;
     prof_mark(ly, 3, st);
     ly->last_launches = launches;
     if (ly->prof_count < ly->prof_max) {
@@ -107,6 +110,7 @@ moe_status forward_impl(moe_layer *ly, const uint16_t *x, const uint16_t *res, u
     int launches = 0;
     const int tdec = decode_max_tokens(L.d);
     if (T > tdec && prefill_supported(L)) return forward_prefill(ly, x, res, out, T, st);
+    ly->y_bf16 = false;
     if (T <= tdec) {
         // the whole layer in one persistent launch
         prof_mark(ly, 0, st);
@@ -260,8 +264,9 @@ moe_status moe_forward_host(moe_layer *ly, const void *x_host, void *out_host, i
 
 moe_status moe_debug_expert_outputs(moe_layer *ly, float *Y, int T, void *stream) {
     if (!ly || !Y || T < 1 || T > ly->L.max_T) return MOE_ERR_INVALID_ARG;
-    size_t bytes = (size_t)T * ly->L.k * ly->L.d * sizeof(float);
-    return cuda_status(cudaMemcpyAsync(Y, ly->ws.Y, bytes, cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
+    const size_t n = (size_t)T * ly->L.k * ly->L.d;
+    if (ly->y_bf16) return cuda_status(launch_bf16_to_f32(ly->ws.xperm, Y, n, (cudaStream_t)stream));
+    return cuda_status(cudaMemcpyAsync(Y, ly->ws.Y, n * sizeof(float), cudaMemcpyDeviceToDevice, (cudaStream_t)stream));
 }
 
 moe_status moe_rmsnorm(const void *x, void *out, int T, int d, float eps, void *stream) {

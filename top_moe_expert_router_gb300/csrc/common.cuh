@@ -351,7 +351,8 @@ cudaError_t launch_decode_fused(const LayerDev &L, const Workspace &ws, const ui
                                 uint16_t *out, int T, cudaStream_t st);
 // misc.cu
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
-                           cudaStream_t st);
+                           cudaStream_t st, bool y_bf16 = false);  // y_bf16: expert outputs in bf16 over ws.xperm
+cudaError_t launch_bf16_to_f32(const uint16_t *in, float *out, size_t n, cudaStream_t st);
 cudaError_t launch_rmsnorm(const uint16_t *x, uint16_t *out, int T, int d, float eps, cudaStream_t st);
 cudaError_t launch_quantize_nvfp4(const uint16_t *W, int n, int rows, int K, uint8_t *q, uint8_t *s, float *g,
                                   cudaStream_t st);

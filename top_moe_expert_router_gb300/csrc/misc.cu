@@ -15,7 +15,17 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // combine: out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] )
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ Y, const float *__restrict__ w,
+// Four consecutive expert outputs at Y + i (fp32, or bf16 when YT = uint16_t).
+__device__ __forceinline__ float4 load_y4(const float *Y, size_t i) {
+    return __ldcg(reinterpret_cast<const float4 *>(Y + i));
+}
+__device__ __forceinline__ float4 load_y4(const uint16_t *Y, size_t i) {
+    const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(Y + i));
+    return make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+}
+
+template <typename YT>
+__global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, const float *__restrict__ w,
                                                       const int32_t *__restrict__ pos,
                                                       const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
                                                       int T, int d, int k, uint32_t *err, int rows) {
@@ -41,7 +51,7 @@ __global__ void __launch_bounds__(256) combine_kernel(const float *__restrict__ 
     float4 y[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j)
-        y[j] = j < k ? __ldcg(reinterpret_cast<const float4 *>(Y + (size_t)rj[j] * d + c)) : make_float4(0, 0, 0, 0);
+        y[j] = j < k ? load_y4(Y, (size_t)rj[j] * d + c) : make_float4(0, 0, 0, 0);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
@@ -141,7 +151,7 @@ __global__ void __launch_bounds__(256) combine_norm_kernel(const float *__restri
 }
 
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
-                           cudaStream_t st) {
+                           cudaStream_t st, bool y_bf16) {
     cudaLaunchConfig_t cfg{};
     if (L.expert_norm) {
         cfg.gridDim = dim3(T);
@@ -163,8 +173,24 @@ cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, combine_kernel, (const float *)ws.Y, (const float *)ws.w,
+    if (y_bf16)
+        return cudaLaunchKernelEx(&cfg, combine_kernel<uint16_t>, (const uint16_t *)ws.xperm, (const float *)ws.w,
+                                  (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
+    return cudaLaunchKernelEx(&cfg, combine_kernel<float>, (const float *)ws.Y, (const float *)ws.w,
                               (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
+}
+
+__global__ void __launch_bounds__(256) bf16_to_f32_kernel(const uint16_t *__restrict__ in, float *__restrict__ out,
+                                                          size_t n) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        out[i] = __uint_as_float((uint32_t)in[i] << 16);
+}
+
+cudaError_t launch_bf16_to_f32(const uint16_t *in, float *out, size_t n, cudaStream_t st) {
+    if (n == 0) return cudaSuccess;
+    const size_t blocks = (n + 255) / 256;
+    bf16_to_f32_kernel<<<(unsigned)(blocks < 4096 ? blocks : 4096), 256, 0, st>>>(in, out, n);
+    return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------

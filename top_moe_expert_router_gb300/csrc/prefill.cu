@@ -35,7 +35,7 @@ constexpr uint32_t kBBytes = BN * BK * 2;       // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr size_t kGemmSmem = 1024 + (size_t)kGemmStages * kStageBytes + 256;
 
-enum { EPI_LOGITS = 0, EPI_SWIGLU = 1, EPI_F32 = 2 };
+enum { EPI_LOGITS = 0, EPI_SWIGLU = 1, EPI_F32 = 2, EPI_BF16 = 3 };
 
 struct GemmParams {
     const int32_t *tile_off;  // [G+1] prefix of 128-row tiles per group; nullptr: one group
@@ -46,7 +46,7 @@ struct GemmParams {
     int K;
     int b_rows_per_group;     // rows of B per group (0 for the router)
     float *out_f32;           // logits [rows, ld] / Y [rows, ld]
-    uint16_t *out_bf16;       // H [rows, ld] (SwiGLU)
+    uint16_t *out_bf16;       // H [rows, ld] (SwiGLU) / Y [rows, ld] (EPI_BF16)
     int ld;                   // output row stride in elements
     int n_valid;              // columns < n_valid are stored (router: E)
     const float *bias;
@@ -310,7 +310,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     tmem_ld16(tbase + j0, v);
                     tmem_ld_wait();
                     const int col0 = ti.n * BN + j0;
-                    if (valid) {
+                    if (valid && EPI == EPI_BF16) {
+                        uint32_t packed[8];
+#pragma unroll
+                        for (int i = 0; i < 8; ++i)
+                            packed[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(v[2 * i])) |
+                                        ((uint32_t)f32_to_bf16_rn(__uint_as_float(v[2 * i + 1])) << 16);
+                        uint4 *dst = reinterpret_cast<uint4 *>(p.out_bf16 + orow * p.ld + col0);
+                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+                    } else if (valid) {
                         float *dst = p.out_f32 + (size_t)ti.ks * p.split_stride + orow * p.ld + col0;
                         if (EPI == EPI_LOGITS) {
                             const bool add_bias = p.bias && ti.ks == 0;  // once, with the first part of K
@@ -434,15 +443,23 @@ cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const
     p.ld = L.I;
     cudaError_t e = launch_gemm<EPI_SWIGLU, true>(ta, tg, tu, p, L.num_sms, st);
     if (e != cudaSuccess) return e;
-    // down: Y = H . Wd^T in fp32
+    // down: Y = H . Wd^T, accumulated in fp32 and stored in bf16 over the
+    // gathered token rows, which the gate/up GEMM no longer needs (fp32 Y for
+    // the per-expert-normalised variant)
     p.nt = L.d / BN;
     p.K = L.I;
     p.b_rows_per_group = L.d;
-    p.out_bf16 = nullptr;
-    p.out_f32 = ws.Y;
     p.ld = L.d;
     p.n_valid = L.d;
-    e = launch_gemm<EPI_F32, false>(th, td, td, p, L.num_sms, st);
+    if (L.expert_norm) {  // the normalising combine reads fp32 Y
+        p.out_bf16 = nullptr;
+        p.out_f32 = ws.Y;
+        e = launch_gemm<EPI_F32, false>(th, td, td, p, L.num_sms, st);
+    } else {
+        p.out_bf16 = ws.xperm;
+        p.out_f32 = nullptr;
+        e = launch_gemm<EPI_BF16, false>(th, td, td, p, L.num_sms, st);
+    }
     *launches += 2;
     return e;
 }
