@@ -95,11 +95,11 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.2e6 + 3.3e6,
+    "decode_t1": {"bytes": 304.22e6 + 3.80e6,
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh"),
-                  "sha256": ("67395a8de9766f652ece05ceb28a5624dbff6347a879bcdb34345b8bffd3e044",
-                             "288137038e4343fe5f67a73751bf0be0bc9b7ff45faf4355d4583f8520766936")},
+                  "sha256": ("8011892625a1d9359ba7a1546b661093603cdf23dbfbd1a0f1388227e7e55e8e",
+                             "86673bf78aa13ea87d52b2615158509ccddf2d2c723433109c951e2f7724e4c0")},
 }
 
 

@@ -228,10 +228,30 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, i
     const int nt = min(kChunk, T - t0);
     for (int i = tid; i < E; i += 256) bm[i] = 0u;
     __syncthreads();
+    __shared__ float s_row[8][256];  // one token's summed logits per warp
     for (int tl = warp; tl < nt; tl += 8) {
         const int t = t0 + tl;
-        topk_warp(ws.logits + (size_t)t * E, E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false, nsplit,
-                  split_stride);
+        // the logits' parts over K: every load issued first, then added in order
+        const float *row = ws.logits + (size_t)t * E;
+        float part[kRouterSplit][8];
+#pragma unroll
+        for (int s = 0; s < kRouterSplit; ++s)
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = lane + 32 * i;
+                part[s][i] = (s < nsplit && e < E) ? row[(size_t)s * split_stride + e] : 0.f;
+            }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane + 32 * i;
+            float l = part[0][i];
+#pragma unroll
+            for (int s = 1; s < kRouterSplit; ++s)
+                if (s < nsplit) l += part[s][i];
+            if (e < E) s_row[warp][e] = l;
+        }
+        __syncwarp();
+        topk_warp(s_row[warp], E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false);
         __syncwarp();
         if (lane < k) {
             const int e = ws.ids[(size_t)t * k + lane];
@@ -252,10 +272,18 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, i
     if (!s_last) return;
     __threadfence();
     const int nch = gridDim.x;
+    // per-chunk counts are read 16 at a time, all loads of a batch issued
+    // before any use: one L2 round trip per batch, not per chunk
+    constexpr int kBatch = 16;
     for (int e = tid; e < E; e += 256) {
         int n = 0;
-#pragma unroll 8
-        for (int cc = 0; cc < nch; ++cc) n += __ldcg(ws.chunk_base + (size_t)cc * E + e);
+        for (int c0 = 0; c0 < nch; c0 += kBatch) {
+            int v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) v[j] = c0 + j < nch ? __ldcg(ws.chunk_base + (size_t)(c0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) n += v[j];
+        }
         s_cnt[e] = n;
         s_flag[e] = n > 0 ? 1 : 0;
     }
@@ -284,11 +312,17 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, i
         ws.counts[e] = s_cnt[e];
         ws.offsets[e] = s_off[e];
         int run = s_off[e];
-        for (int cc = 0; cc < nch; ++cc) {   // chunk counts -> first row of each chunk
-            const size_t i = (size_t)cc * E + e;
-            const int n = __ldcg(ws.chunk_base + i);
-            ws.chunk_base[i] = run;
-            run += n;
+        for (int c0 = 0; c0 < nch; c0 += kBatch) {   // chunk counts -> first row of each chunk
+            int v[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) v[j] = c0 + j < nch ? __ldcg(ws.chunk_base + (size_t)(c0 + j) * E + e) : 0;
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j) {
+                if (c0 + j < nch) {
+                    ws.chunk_base[(size_t)(c0 + j) * E + e] = run;
+                    run += v[j];
+                }
+            }
         }
     }
 }
