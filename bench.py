@@ -448,8 +448,14 @@ def run_stack(args, w, moe, device, dist, rank, world, local_rank):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream()
 
+    # the whole stack in one launch when the batch fits (T <= 8)
+    stack = moe.MoeStack(layers) if w.T <= 8 else None
+
     def step(x0, route_log=None):
         xcur.copy_(x0)
+        if stack is not None and route_log is None:
+            stack.forward(xcur, out=xcur, eps=1e-6)
+            return
         for gl in layers:
             moe.rmsnorm(xcur, 1e-6, out=ubuf)
             if route_log is not None:
@@ -474,13 +480,13 @@ def run_stack(args, w, moe, device, dist, rank, world, local_rank):
         evs[s][0].record(stream)
         step(pool[s % POOL])
         evs[s][1].record(stream)
-        launches += w.layers * (1 + layers[0].last_launch_count())
+        launches += 1 if stack is not None else w.layers * (1 + layers[0].last_launch_count())
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
     clk = clocks.stop()
     step_ms = np.array([a.elapsed_time(b) for a, b in evs])
-    profs = [gl.profile_end() for gl in layers]             # each [steps, 4]
+    profs = [gl.profile_end() for gl in layers]             # each [steps, 4] (empty for the stacked launch)
     for gl in layers:
         assert gl.device_status() == 0
     total_s = float(step_ms.sum()) / 1e3
@@ -497,7 +503,14 @@ def run_stack(args, w, moe, device, dist, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     hbm = peaks["hbm_gbs"]
     layer_bytes = Us * eb + w.E * w.d * 2                           # [steps, layers]
-    if profs[0].shape[1] == 1:
+    if stack is not None:
+        # one stacked launch per step: its bytes are all layers' bytes, its
+        # time the step's (the step adds one 32 KB token copy)
+        kname = f"decode_layer_kernel (NVFP4, {w.layers} layers in one launch)"
+        k_bytes = layer_bytes.sum(1, keepdims=True)
+        k_ms = step_ms[:, None].astype(np.float64)
+        kms = {"stack": float(k_ms.mean()), "per_layer": float(k_ms.mean() / w.layers)}
+    elif profs[0].shape[1] == 1:
         kname = "decode_layer_kernel (NVFP4)"
         k_bytes = layer_bytes
         k_ms = np.stack([p[:, 0] for p in profs], axis=1).astype(np.float64)
@@ -520,7 +533,7 @@ def run_stack(args, w, moe, device, dist, rank, world, local_rank):
             "data": "synthetic",
             "config": workload_config(w, parallelism=f"replicas x{world}",
                                       l2="flushed before every step (256 MiB write), outside the step events",
-                                      step="8 x (RMSNorm, MoE, residual)"),
+                                      step="8 x (RMSNorm, MoE, residual)" + (", one launch" if stack is not None else "")),
             "roofline": {"kernel": kname, "bound": "hbm", "achieved": gu_gbs, "peak": hbm,
                          "unit": "GB/s", "frac": gu_gbs / hbm, "traffic": None, "peak_source": peak_src,
                          "bytes_per_launch": float(gu_bytes.mean()), "ms_per_launch": float(gu_ms.mean())},

@@ -187,6 +187,29 @@ moe_status moe_profile_end(moe_layer *layer, float *ms_host, int max_kernels, in
 moe_status moe_forward_static_scratch(const moe_layer_desc *desc, const void *x, void *out, int T,
                                       void *stream);
 
+/* Stacked layers in one launch (the persistent multi-layer decode kernel
+ * the pages' megakernel idea suggests, "How SGLang-TorchTPU accelerated an
+ * 816B-parameter MoE on TPU v7", section "Key optimisations"). For
+ * l = 0 .. n_layers-1:
+ *     x_{l+1} = x_l + MoE_l(RMSNorm(x_l)),   x_0 = x,   out = x_n,
+ * RMSNorm without a gain, eps as given, its output rounded to bf16 (the
+ * arithmetic of moe_rmsnorm), the sum rounded to bf16 (moe_forward_residual).
+ * - moe_stack_create: 1 <= n_layers <= 64 layers of equal d, E, top_k, I and
+ *   weight format, without expert_out_norm, whose max_tokens >= 1. It writes
+ *   the layers' weight pointers (not the weights) into layers[0]'s workspace
+ *   once (a synchronous copy); the stack then runs on that workspace, so the
+ *   stack and layers[0] must not run at the same time. The layers must
+ *   outlive the stack.
+ * - moe_stack_forward: T in [1, 8] and <= layers[0]'s max_tokens; x, out bf16
+ *   [T, d] device buffers (out may alias x). layer_out, if not NULL, receives
+ *   every layer's output, [n_layers, T, d] bf16. One launch, no host sync.
+ *   Errors as for moe_forward. */
+typedef struct moe_stack moe_stack;
+moe_status moe_stack_create(moe_layer *const *layers, int n_layers, moe_stack **out);
+moe_status moe_stack_forward(moe_stack *stack, const void *x, void *out, int T, float eps, void *layer_out,
+                             void *stream);
+moe_status moe_stack_destroy(moe_stack *stack);
+
 moe_status moe_layer_destroy(moe_layer *layer);
 
 const char *moe_status_string(moe_status s);

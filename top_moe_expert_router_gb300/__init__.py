@@ -81,6 +81,9 @@ def load(path: str | None = None):
             "moe_profile_end": ([vp, vp, i, ctypes.POINTER(i), ctypes.POINTER(i)], st),
             "moe_layer_destroy": ([vp], st),
             "moe_forward_static_scratch": ([ctypes.POINTER(MoeLayerDesc), vp, vp, i, vp], st),
+            "moe_stack_create": ([ctypes.POINTER(vp), i, ctypes.POINTER(vp)], st),
+            "moe_stack_forward": ([vp, vp, vp, i, f, vp, vp], st),
+            "moe_stack_destroy": ([vp], st),
             "moe_status_string": ([st], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
@@ -224,6 +227,40 @@ class MoeLayer:
     def close(self):
         if getattr(self, "_h", None):
             load().moe_layer_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+class MoeStack:
+    """Layers of equal shape run in one launch: x <- x + MoE_l(RMSNorm(x)) for
+    each layer in order (moe_stack_forward). The stack runs on the first
+    layer's workspace; keep the layers alive while the stack is used."""
+
+    def __init__(self, layers):
+        self.layers = list(layers)
+        handles = (ctypes.c_void_p * len(self.layers))(*[ly._h.value for ly in self.layers])
+        h = ctypes.c_void_p()
+        _check(load().moe_stack_create(handles, len(self.layers), ctypes.byref(h)), "moe_stack_create")
+        self._h = h
+        self.d = self.layers[0].d
+
+    def forward(self, x, out=None, eps=1e-6, layer_out=None, stream=None):
+        _require_cuda(x, out, layer_out)
+        T = x.shape[0]
+        if out is None:
+            out = torch.empty((T, self.d), dtype=torch.bfloat16, device=x.device)
+        _check(load().moe_stack_forward(self._h, _ptr(x), _ptr(out), T, float(eps), _ptr(layer_out),
+                                        _stream(stream)), "moe_stack_forward")
+        return out
+
+    def close(self):
+        if getattr(self, "_h", None) is not None:
+            load().moe_stack_destroy(self._h)
             self._h = None
 
     def __del__(self):

@@ -328,6 +328,50 @@ moe_status moe_profile_end(moe_layer *ly, float *ms, int max_kernels, int *n_for
     return s;
 }
 
+struct moe_stack {
+    moe_layer *first;  // its workspace holds the stack's weight records
+    int n_layers;
+};
+
+moe_status moe_stack_create(moe_layer *const *layers, int n_layers, moe_stack **out) {
+    if (!layers || !out || n_layers < 1 || n_layers > kMaxStack) return MOE_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (!layers[0]) return MOE_ERR_INVALID_ARG;
+    const LayerDev &L0 = layers[0]->L;
+    std::vector<LayerW> w((size_t)n_layers);
+    for (int l = 0; l < n_layers; ++l) {
+        const moe_layer *ly = layers[l];
+        if (!ly) return MOE_ERR_INVALID_ARG;
+        const LayerDev &L = ly->L;
+        if (L.d != L0.d || L.E != L0.E || L.k != L0.k || L.I != L0.I || L.fmt != L0.fmt) return MOE_ERR_INVALID_ARG;
+        if (L.expert_norm) return MOE_ERR_UNSUPPORTED;
+        w[(size_t)l] = LayerW{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+    }
+    if (cudaMemcpy(layers[0]->ws.stack, w.data(), sizeof(LayerW) * (size_t)n_layers, cudaMemcpyHostToDevice) !=
+        cudaSuccess)
+        return MOE_ERR_CUDA;
+    *out = new moe_stack{layers[0], n_layers};
+    return MOE_OK;
+}
+
+moe_status moe_stack_forward(moe_stack *sk, const void *x, void *out, int T, float eps, void *layer_out,
+                             void *stream) {
+    if (!sk || !x || !out || !aligned16(x) || !aligned16(out) || (layer_out && !aligned16(layer_out)) || T < 1 ||
+        T > 8 || T > sk->first->L.max_T || !(eps >= 0.f))
+        return MOE_ERR_INVALID_ARG;
+    moe_layer *ly = sk->first;
+    const cudaError_t e = launch_decode_stack(ly->L, ly->ws, sk->n_layers, eps, (const uint16_t *)x,
+                                              (uint16_t *)out, (uint16_t *)layer_out, T, (cudaStream_t)stream);
+    ly->last_launches = 1;
+    if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) return MOE_ERR_UNSUPPORTED;
+    return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_stack_destroy(moe_stack *sk) {
+    delete sk;
+    return MOE_OK;
+}
+
 moe_status moe_layer_destroy(moe_layer *ly) {
     if (ly)
         for (cudaEvent_t ev : ly->prof_events) cudaEventDestroy(ev);

@@ -54,8 +54,21 @@ inline int router_ksplit(int d) {
     return kb % kRouterSplit == 0 ? kRouterSplit : (kb % 2 == 0 ? 2 : 1);
 }
 
+// One layer's weights, as the kernels see them (bf16 or NVFP4 fields used).
+struct LayerW {
+    const uint16_t *wr;       // [E, d] router
+    const float *bias;        // [E] or null
+    const uint16_t *wg, *wu, *wd;
+    const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
+    const float *gg, *gu, *gd;
+};
+
+// Layers one stacked launch can run.
+constexpr int kMaxStack = 64;
+
 struct Workspace {
     Control *ctrl;
+    LayerW *stack;      // [kMaxStack] weights of the layers of a stacked launch
     float *logits;      // [kRouterSplit][max_T, E] (decode: the first slice)
     int32_t *ids;       // [max_T, k]
     float *w;           // [max_T, k]
@@ -88,6 +101,7 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     };
     size_t Tk = (size_t)max_T * k;
     ws.ctrl = (Control *)take(sizeof(Control));
+    ws.stack = (LayerW *)take(sizeof(LayerW) * kMaxStack);
     ws.logits = (float *)take(sizeof(float) * (size_t)kRouterSplit * max_T * E);
     ws.ids = (int32_t *)take(sizeof(int32_t) * Tk);
     ws.w = (float *)take(sizeof(float) * Tk);
@@ -201,6 +215,11 @@ __device__ __forceinline__ void fence_acq_rel_gpu() { asm volatile("fence.acq_re
 
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Ends an mbarrier's life so that its word can be initialised again.
+__device__ __forceinline__ void mbar_inval(uint64_t *bar) {
+    asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Makes mbarrier initialisation visible to the async (TMA) proxy.
@@ -349,6 +368,10 @@ cudaError_t launch_decode_down(const LayerDev &L, const Workspace &ws, const uin
 // decode_fused.cu
 cudaError_t launch_decode_fused(const LayerDev &L, const Workspace &ws, const uint16_t *x, const uint16_t *res,
                                 uint16_t *out, int T, cudaStream_t st);
+// n_layers stacked layers (weights in ws.stack, shapes of L) in one launch:
+// x_{l+1} = x_l + MoE_l(RMSNorm(x_l)), x_0 = x, out = x_n; T <= 8.
+cudaError_t launch_decode_stack(const LayerDev &L, const Workspace &ws, int n_layers, float eps, const uint16_t *x,
+                                uint16_t *out, uint16_t *layer_out, int T, cudaStream_t st);
 // misc.cu
 cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_t *res, uint16_t *out, int T,
                            cudaStream_t st, bool y_bf16 = false);  // y_bf16: expert outputs in bf16 over ws.xperm

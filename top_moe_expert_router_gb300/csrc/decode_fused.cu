@@ -1,1269 +1,8 @@
-// decode_fused.cu — one persistent kernel for a whole small-batch (T <= 16)
-// MoE layer: router, softmax/top-k/renormalise, permutation, the expert
-// weight stream through gate/up and down, and the weighted combine.
-//
-// Decode is bound by streaming weights from HBM and by the boundaries
-// between kernels, which break the overlap of weight streaming and compute
-// ("How SGLang-TorchTPU accelerated an 816B-parameter MoE on TPU v7",
-// sections "Introduction" and "Key optimisations"). Here the layer is one
-// cooperative launch, one CTA per SM:
-//   1. router: every CTA computes the logits of its experts (x . Wr[e]),
-//      grid barrier;
-//   2. routing: every CTA computes top-k and the permutation of all T tokens
-//      itself, in shared memory (identical results everywhere; CTA 0 also
-//      publishes them), so no second barrier is needed;
-//   3. one producer lane fills a ring of shared-memory slots with bulk TMA
-//      copies: first this CTA's share of the active experts' gate/up rows,
-//      then, without a pause, its share of their down rows; slot j belongs
-//      to consumer warp j % c, which takes the slot's phases in order;
-//   4. consumer warps compute h = silu(Wg x) * (Wu x) (fp32, to global) and
-//      count the rows in, per half of the active experts; the stream runs
-//      first-half gate/up, second-half gate/up, first-half down, second-half
-//      down, so a half's h is complete long before its down rows arrive and
-//      the weight stream never pauses; then Y = Wd h (fp32, to global);
-//   5. combine: per 256-column block of the output, the CTA whose down rows
-//      complete the block (a row counter per block) forms
-//      out = (res +) sum_j w_j Y_j for those columns, in fp32, j ascending.
-// Every wait (mbarrier, grid barrier) is bounded; a timeout sets the error
-// word and the kernel unwinds.
-#include <cuda_fp4.h>
-#include <cuda_fp8.h>
-#include <cuda_runtime.h>
-
-#include "common.cuh"
+// decode_fused.cu — the single-layer instantiations of the persistent
+// small-batch layer kernel (decode_fused.cuh) and their launcher.
+#include "decode_fused.cuh"
 
 namespace moe {
-
-namespace fused {
-
-// Warps per CTA: 7 consumers and the producer. Registers are handed out per
-// group of four warps, so a CTA of 4n warps wastes none; a 9-warp CTA would be
-// charged for 12 (capping a thread at 168 registers). (12-warp NVFP4 CTAs
-// were measured slower: fewer ring slots per consumer and fewer producer lanes.)
-template <int TM, bool FP4>
-struct Warps {
-    static constexpr int kWarps = 8;
-    static constexpr int kThreads = 32 * kWarps;
-    static constexpr int kConsumers = kWarps - 1;   // consumer warps at most
-    static constexpr int kProducerWarp = kWarps - 1;
-};
-constexpr int kDnRows = 4;                    // down rows per stage
-constexpr int kMaxSlots = 32;
-constexpr int kSmemBudget = 227 * 1024;
-constexpr int kCb = 256;                      // output columns per combine block
-
-struct Args {
-    const uint16_t *x;        // [T, d] bf16
-    const uint16_t *res;      // [T, d] bf16 or null
-    uint16_t *out;            // [T, d] bf16
-    const uint16_t *wr;       // [E, d]
-    const float *bias;        // [E] or null
-    const uint16_t *wg, *wu, *wd;
-    const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
-    const float *gg, *gu, *gd;
-    int T, d, I, E, k;
-    int nslots, ncons, nprod;
-    uint32_t slot_bytes;
-    int x_in_smem;            // tokens' rows staged in shared memory
-    int x_router_ring;        // no room for that: the router reads them from the (still idle) ring
-    int do_combine;           // 0: leave Y for a separate combine kernel
-    Workspace ws;
-};
-
-template <bool FP4>
-__host__ __device__ constexpr uint32_t rowb(int K) {
-    return FP4 ? (uint32_t)K / 2 + (uint32_t)K / 16 : (uint32_t)K * 2;
-}
-
-// ---------------------------------------------------------------------------
-// small helpers
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ float2 bf2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
-
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return __ffma2_rn(a, b, c); }
-
-__device__ __forceinline__ void fp4x16(uint2 q, float2 f[8]) {
-    const uint32_t words[2] = {q.x, q.y};
-#pragma unroll
-    for (int wi = 0; wi < 2; ++wi)
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((words[wi] >> (8 * b)) & 0xFFu),
-                                                       __NV_E2M1);
-            f[wi * 4 + b] = __half22float2(*reinterpret_cast<__half2 *>(&hr));
-        }
-}
-
-__device__ __forceinline__ float e4m3f(uint8_t s) {
-    __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)s, __NV_E4M3);
-    return __half2float(*reinterpret_cast<__half *>(&hr));
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid barrier over all CTAs of the (cooperative) launch: arrival counter
-// `target` = (barrier index) x (grid size). Bounded wait.
-__device__ bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, volatile int *abort_flag) {
-    __syncthreads();
-    __shared__ int ok;
-    if (threadIdx.x == 0) {
-        fence_acq_rel_gpu();
-        atomicAdd(ctr, 1u);
-        ok = 1;
-        unsigned long long t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(err, ERRBIT_TIMEOUT);
-                *abort_flag = 1;
-                ok = 0;
-                break;
-            }
-        }
-        fence_acq_rel_gpu();
-    }
-    __syncthreads();
-    return ok != 0;
-}
-
-// This CTA's stages: segment A = first-half gate/up row pairs, B = second-half
-// gate/up, C = first-half down units (kDnRows rows), D = second-half down.
-struct Plan {
-    int nA, nB, nC, nD;        // stages of each segment in this CTA
-    int a0, b0, c0, d0;        // first index of this CTA's share within each segment
-    int offB, offD;            // global start of the second-half segments
-    // flattened gate/up row-pair index (u * I + i) of gate/up stage s
-    __device__ __forceinline__ int gu_row(int s) const { return s < nA ? a0 + s : offB + b0 + (s - nA); }
-    // flattened down unit index (u * d / kDnRows + c / kDnRows) of down stage t (t = s - nA - nB)
-    __device__ __forceinline__ int dn_unit(int t) const { return t < nC ? c0 + t : offD + d0 + (t - nC); }
-};
-
-__device__ __forceinline__ void share(int total, int b, int G, int &start, int &count) {
-    start = (int)((long long)b * total / G);
-    count = (int)((long long)(b + 1) * total / G) - start;
-}
-
-__device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, int b, int G) {
-    Plan p;
-    const int U1 = (U + 1) / 2, U2 = U - U1;
-    share(U1 * I, b, G, p.a0, p.nA);
-    share(U2 * I, b, G, p.b0, p.nB);
-    share(U1 * units_per_expert, b, G, p.c0, p.nC);
-    share(U2 * units_per_expert, b, G, p.d0, p.nD);
-    p.offB = U1 * I;
-    p.offD = U1 * units_per_expert;
-    return p;
-}
-
-// Cost of one stage of an expert with n tokens, in arbitrary units: every
-// stage streams the same bytes, but in a multi-token batch the arithmetic,
-// which grows with the tokens, sets the pace. Measured at 4 and 16 tokens
-// (costs 2 + n, 1 + n, 1 + 2n, n and a steeper 3n tried), n balances best.
-__device__ __forceinline__ int stage_weight(int n) { return n; }
-
-// Index, within a segment of experts [u_lo, u_hi) holding `per` stages each,
-// where CTA bb's share starts when the segment is cut into G parts of equal
-// total weight (bb = G gives the segment's end). cw: exclusive prefix over
-// experts of one stage's weight.
-__device__ __forceinline__ int weighted_start(const int32_t *cw, int u_lo, int u_hi, int per, int bb, int G) {
-    if (u_hi <= u_lo) return 0;
-    if (bb >= G) return (u_hi - u_lo) * per;
-    const long long base = cw[u_lo];
-    const long long t = (long long)(cw[u_hi] - base) * per * bb / G;
-    int lo = u_lo, hi = u_hi;  // the expert holding weight position t
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if ((long long)(cw[mid] - base) * per <= t)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    const long long w = cw[lo + 1] - cw[lo];
-    const long long j = (t - (long long)(cw[lo] - base) * per + w - 1) / w;
-    return (lo - u_lo) * per + (int)(j < per ? j : per);
-}
-
-// make_plan with the segments cut by weight instead of by stage count.
-__device__ __forceinline__ Plan make_plan_weighted(const int32_t *cw, int U, int I, int units_per_expert, int b,
-                                                   int G) {
-    Plan p;
-    const int U1 = (U + 1) / 2;
-    p.a0 = weighted_start(cw, 0, U1, I, b, G);
-    p.nA = weighted_start(cw, 0, U1, I, b + 1, G) - p.a0;
-    p.b0 = weighted_start(cw, U1, U, I, b, G);
-    p.nB = weighted_start(cw, U1, U, I, b + 1, G) - p.b0;
-    p.c0 = weighted_start(cw, 0, U1, units_per_expert, b, G);
-    p.nC = weighted_start(cw, 0, U1, units_per_expert, b + 1, G) - p.c0;
-    p.d0 = weighted_start(cw, U1, U, units_per_expert, b, G);
-    p.nD = weighted_start(cw, U1, U, units_per_expert, b + 1, G) - p.d0;
-    p.offB = U1 * I;
-    p.offD = U1 * units_per_expert;
-    return p;
-}
-
-// Publish a warp's count of finished h rows (all lanes' h stores first).
-__device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
-    fence_acq_rel_gpu();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0 && n) atomicAdd(ctr, (uint32_t)n);
-}
-
-// Warp-wide bounded wait until *ctr >= target.
-__device__ __forceinline__ bool wait_rows(const uint32_t *ctr, uint32_t target, uint32_t *err,
-                                          volatile int *abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(err, ERRBIT_TIMEOUT);
-                *abort_flag = 1;
-                ok = 0;
-                break;
-            }
-        }
-    }
-    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
-// Sums of four rows' per-lane partials (one token), reduced together:
-// exchanging halves, lane group q (lanes 8q .. 8q+7) ends with row q, and its
-// first lane stores y[q] = sum * scale.
-__device__ __forceinline__ void store_four_rows(float r0, float r1, float r2, float r3, float *y, float scale) {
-    const int lane = threadIdx.x & 31;
-    const bool hi16 = lane & 16, hi8 = lane & 8;
-    // lanes < 16 keep rows 0,1; lanes >= 16 keep rows 2,3
-    float k0 = hi16 ? r2 : r0, k1 = hi16 ? r3 : r1;
-    const float s0 = hi16 ? r0 : r2, s1 = hi16 ? r1 : r3;
-    k0 += __shfl_xor_sync(0xFFFFFFFFu, s0, 16);
-    k1 += __shfl_xor_sync(0xFFFFFFFFu, s1, 16);
-    // within each half, lanes with bit 3 clear keep the first of the two rows
-    float k = hi8 ? k1 : k0;
-    k += __shfl_xor_sync(0xFFFFFFFFu, hi8 ? k0 : k1, 8);
-    k += __shfl_xor_sync(0xFFFFFFFFu, k, 4);
-    k += __shfl_xor_sync(0xFFFFFFFFu, k, 2);
-    k += __shfl_xor_sync(0xFFFFFFFFu, k, 1);
-    if ((lane & 7) == 0) y[lane >> 3] = k * scale;
-}
-
-// Per-warp cache of the expert a stage belongs to (read from shared memory).
-template <int TM>
-struct Seg {
-    int u = -1, e = 0, n_e = 0, row0 = 0;
-    int tok[TM];
-};
-
-// Routing state in shared memory.
-struct Route {
-    int32_t *ids, *pos, *perm, *cnt, *off, *uniq, *scan;
-    float *w;
-    uint32_t *bm;
-    int *n_uniq;
-};
-
-template <int TM>
-__device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
-    s.u = u;
-    s.e = R.uniq[u];
-    s.n_e = R.cnt[s.e] < TM ? R.cnt[s.e] : TM;
-    s.row0 = R.off[s.e];
-#pragma unroll
-    for (int r = 0; r < TM; ++r) s.tok[r] = r < s.n_e ? R.perm[s.row0 + r] : 0;
-}
-
-// exclusive scan of a[0..n) (n <= 256) by one warp; returns the total
-__device__ int warp_scan256(const int32_t *a, int32_t *out, int n) {
-    const int lane = threadIdx.x & 31;
-    int vals[8], local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        vals[i] = idx < n ? a[idx] : 0;
-        local += vals[i];
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int run = incl - local;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        if (idx < n) out[idx] = run;
-        run += vals[i];
-    }
-    return __shfl_sync(0xFFFFFFFFu, incl, 31);
-}
-
-// One gate/up stage (the row pair i of expert seg.e in `st`) for an expert
-// with NE tokens at most (seg.n_e <= NE; exactly NE when NE <= 2): h rows of
-// its tokens, h = silu(g) * u. Releases the slot once the stage is read.
-template <int NE, int TM, bool FP4>
-__device__ __forceinline__ void gu_stage(const Args &a, const unsigned char *st, const unsigned char *xs,
-                                         const float *xscale, const Seg<TM> &seg, uint64_t *empty_slot, int i) {
-    const int lane = threadIdx.x & 31;
-    const int d = a.d, I = a.I;
-    const uint32_t rbg = rowb<FP4>(d);
-    float2 ag[NE], au[NE];
-#pragma unroll
-    for (int r = 0; r < NE; ++r) ag[r] = au[r] = make_float2(0.f, 0.f);
-    if (!FP4) {
-        constexpr int kXV = 8;
-        const uint4 *gw = reinterpret_cast<const uint4 *>(st);
-        const uint4 *uw = reinterpret_cast<const uint4 *>(st + rbg);
-        const int nvec = d / 8;
-        if (a.x_in_smem) {
-            // vector by vector: each weight vector is unpacked once and
-            // used for every token of the expert
-#pragma unroll 2
-            for (int v = lane; v < nvec; v += 32) {
-                const uint4 g4 = gw[v], u4 = uw[v];
-                const float2 g0 = bf2(g4.x), g1 = bf2(g4.y), g2 = bf2(g4.z), g3 = bf2(g4.w);
-                const float2 u0 = bf2(u4.x), u1 = bf2(u4.y), u2 = bf2(u4.z), u3 = bf2(u4.w);
-#pragma unroll
-                for (int r = 0; r < NE; ++r) {
-                    if (NE <= 2 || r < seg.n_e) {
-                        const uint4 xv = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)[v];
-                        const float2 x0 = bf2(xv.x), x1 = bf2(xv.y), x2 = bf2(xv.z), x3 = bf2(xv.w);
-                        ag[r] = ffma2(g0, x0, ag[r]);
-                        au[r] = ffma2(u0, x0, au[r]);
-                        ag[r] = ffma2(g1, x1, ag[r]);
-                        au[r] = ffma2(u1, x1, au[r]);
-                        ag[r] = ffma2(g2, x2, ag[r]);
-                        au[r] = ffma2(u2, x2, au[r]);
-                        ag[r] = ffma2(g3, x3, ag[r]);
-                        au[r] = ffma2(u3, x3, au[r]);
-                    }
-                }
-            }
-        } else {
-        // token by token; each lane's vectors in chunks of kXV whose
-        // token loads (from global memory) are all issued before the
-        // arithmetic: one latency per chunk
-#pragma unroll
-        for (int r = 0; r < NE; ++r) {
-            if (NE <= 2 || r < seg.n_e) {
-                const uint4 *xrow = a.x_in_smem
-                                        ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2)
-                                        : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d);
-                for (int j0 = 0; j0 * 32 < nvec; j0 += kXV) {
-                    uint4 xv[kXV];
-#pragma unroll
-                    for (int jj = 0; jj < kXV; ++jj) {
-                        const int v = lane + 32 * (j0 + jj);
-                        xv[jj] = v < nvec ? (a.x_in_smem ? xrow[v] : __ldg(xrow + v)) : make_uint4(0, 0, 0, 0);
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < kXV; ++jj) {
-                        const int v = lane + 32 * (j0 + jj);
-                        if (v < nvec) {
-                            const uint4 g4 = gw[v], u4 = uw[v];
-                            const float2 x0 = bf2(xv[jj].x), x1 = bf2(xv[jj].y), x2 = bf2(xv[jj].z),
-                                         x3 = bf2(xv[jj].w);
-                            ag[r] = ffma2(bf2(g4.x), x0, ag[r]);
-                            au[r] = ffma2(bf2(u4.x), x0, au[r]);
-                            ag[r] = ffma2(bf2(g4.y), x1, ag[r]);
-                            au[r] = ffma2(bf2(u4.y), x1, au[r]);
-                            ag[r] = ffma2(bf2(g4.z), x2, ag[r]);
-                            au[r] = ffma2(bf2(u4.z), x2, au[r]);
-                            ag[r] = ffma2(bf2(g4.w), x3, ag[r]);
-                            au[r] = ffma2(bf2(u4.w), x3, au[r]);
-                        }
-                    }
-                }
-            }
-        }
-        }
-    } else {
-        const unsigned char *gq = st, *gs = st + d / 2, *uq = st + rbg, *us = st + rbg + d / 2;
-        if (a.x_in_smem) {
-            // tokens in shared memory as fp16(x / max|x|): the 16 products
-            // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
-            // pairs, then scaled by the block scale and max|x| in fp32
-            float xsc[NE];  // per-token max|x|
-#pragma unroll
-            for (int r = 0; r < NE; ++r) xsc[r] = (NE <= 2 || r < seg.n_e) ? xscale[seg.tok[r]] : 0.f;
-#pragma unroll 2
-            for (int bb = lane; bb < d / 16; bb += 32) {
-                const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
-                const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
-                __half2 gh[8], uh[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t gw_ = q < 4 ? gqv.x : gqv.y, uw_ = q < 4 ? uqv.x : uqv.y;
-                    __half2_raw g2 = __nv_cvt_fp4x2_to_halfraw2(
-                        (__nv_fp4x2_storage_t)((gw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                    __half2_raw u2 = __nv_cvt_fp4x2_to_halfraw2(
-                        (__nv_fp4x2_storage_t)((uw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                    gh[q] = *reinterpret_cast<__half2 *>(&g2);
-                    uh[q] = *reinterpret_cast<__half2 *>(&u2);
-                }
-                const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
-#pragma unroll
-                for (int r = 0; r < NE; ++r) {
-                    if (NE <= 2 || r < seg.n_e) {
-                        const uint4 *xp = reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2;
-                        const uint4 xa = xp[0], xb = xp[1];
-                        const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                        // two chains per matrix (even / odd pairs), joined at the end
-                        __half2 pg0 = __hmul2(gh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
-                        __half2 pu0 = __hmul2(uh[0], *reinterpret_cast<const __half2 *>(&xw[0]));
-                        __half2 pg1 = __hmul2(gh[1], *reinterpret_cast<const __half2 *>(&xw[1]));
-                        __half2 pu1 = __hmul2(uh[1], *reinterpret_cast<const __half2 *>(&xw[1]));
-#pragma unroll
-                        for (int q = 2; q < 8; q += 2) {
-                            pg0 = __hfma2(gh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pg0);
-                            pu0 = __hfma2(uh[q], *reinterpret_cast<const __half2 *>(&xw[q]), pu0);
-                            pg1 = __hfma2(gh[q + 1], *reinterpret_cast<const __half2 *>(&xw[q + 1]), pg1);
-                            pu1 = __hfma2(uh[q + 1], *reinterpret_cast<const __half2 *>(&xw[q + 1]), pu1);
-                        }
-                        const float2 fg = __half22float2(__hadd2(pg0, pg1)), fu = __half22float2(__hadd2(pu0, pu1));
-                        ag[r].x = fmaf(fg.x + fg.y, sgb * xsc[r], ag[r].x);
-                        au[r].x = fmaf(fu.x + fu.y, sub * xsc[r], au[r].x);
-                    }
-                }
-            }
-        } else
-        for (int bb = lane; bb < d / 16; bb += 32) {
-            float2 gf[8], uf[8];
-            fp4x16(*reinterpret_cast<const uint2 *>(gq + bb * 8), gf);
-            fp4x16(*reinterpret_cast<const uint2 *>(uq + bb * 8), uf);
-            const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
-#pragma unroll
-            for (int r = 0; r < NE; ++r) {
-                if (NE <= 2 || r < seg.n_e) {
-                    const uint4 *xp =
-                        a.x_in_smem ? reinterpret_cast<const uint4 *>(xs + (size_t)seg.tok[r] * d * 2) + bb * 2
-                                    : reinterpret_cast<const uint4 *>(a.x + (size_t)seg.tok[r] * d) + bb * 2;
-                    const uint4 xa = a.x_in_smem ? xp[0] : __ldg(xp), xb = a.x_in_smem ? xp[1] : __ldg(xp + 1);
-                    const uint32_t xw[8] = {xa.x, xa.y, xa.z, xa.w, xb.x, xb.y, xb.z, xb.w};
-                    float2 pg = make_float2(0.f, 0.f), pu = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const float2 xq = bf2(xw[q]);
-                        pg = ffma2(gf[q], xq, pg);
-                        pu = ffma2(uf[q], xq, pu);
-                    }
-                    ag[r].x = fmaf(pg.x + pg.y, sgb, ag[r].x);
-                    au[r].x = fmaf(pu.x + pu.y, sub, au[r].x);
-                }
-            }
-        }
-    }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(empty_slot);
-    const float gsc = FP4 ? a.gg[seg.e] : 1.f, usc = FP4 ? a.gu[seg.e] : 1.f;
-    if (seg.n_e == 1) {
-        // one token: lanes < 16 reduce the gate sum, lanes >= 16 the up sum
-        const bool hi = lane & 16;
-        const float gs_ = ag[0].x + ag[0].y, us_ = au[0].x + au[0].y;
-        float kk = hi ? us_ : gs_;
-        kk += __shfl_xor_sync(0xFFFFFFFFu, hi ? gs_ : us_, 16);
-        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 8);
-        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 4);
-        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 2);
-        kk += __shfl_xor_sync(0xFFFFFFFFu, kk, 1);
-        const float up_total = __shfl_sync(0xFFFFFFFFu, kk, 16);
-        if (lane == 0) a.ws.h[(size_t)seg.row0 * I + i] = silu(kk * gsc) * (up_total * usc);
-    } else {
-        float hv = 0.f;
-#pragma unroll
-        for (int r = 0; r < NE; ++r) {
-            if (NE <= 2 || r < seg.n_e) {
-                const float sg_ = warp_sum(ag[r].x + ag[r].y) * gsc;
-                const float su_ = warp_sum(au[r].x + au[r].y) * usc;
-                if (lane == r) hv = silu(sg_) * su_;
-            }
-        }
-        if (lane < seg.n_e) a.ws.h[(size_t)(seg.row0 + lane) * I + i] = hv;
-    }
-}
-
-// Down rows of one stage (kDnRows rows of W_down in `st`) for a group of nr
-// tokens of one expert (nr <= NG; exactly NG when NG <= 2), h rows at hg:
-// y[t][q] for the group's tokens t, stored at yg[t * d + q] (scaled by gsc).
-template <int NG, bool FP4>
-__device__ __forceinline__ void dn_group(const Args &a, const unsigned char *st, const float *hg, int nr, float *yg,
-                                         float gsc) {
-    const int lane = threadIdx.x & 31;
-    const int d = a.d, I = a.I;
-    const int nvec = I / 8;
-    const uint32_t rbd = rowb<FP4>(I);
-    float2 acc[kDnRows][NG];
-#pragma unroll
-    for (int q = 0; q < kDnRows; ++q)
-#pragma unroll
-        for (int r = 0; r < NG; ++r) acc[q][r] = make_float2(0.f, 0.f);
-    if (!FP4) {
-        // token by token; h (in L2, written by other CTAs) fetched
-        // in chunks of kHV vectors per lane, all loads of a chunk
-        // issued before its arithmetic
-        constexpr int kHV = 4;
-#pragma unroll
-        for (int r = 0; r < NG; ++r) {
-            if (NG <= 2 || r < nr) {
-                const float4 *hr = reinterpret_cast<const float4 *>(hg + (size_t)r * I);
-                for (int j0 = 0; j0 * 32 < nvec; j0 += kHV) {
-                    float4 h0[kHV], h1[kHV];
-#pragma unroll
-                    for (int jj = 0; jj < kHV; ++jj) {
-                        const int v = lane + 32 * (j0 + jj);
-                        if (v < nvec) {
-                            h0[jj] = __ldcg(hr + 2 * v);
-                            h1[jj] = __ldcg(hr + 2 * v + 1);
-                        }
-                    }
-#pragma unroll
-                    for (int jj = 0; jj < kHV; ++jj) {
-                        const int v = lane + 32 * (j0 + jj);
-                        if (v < nvec) {
-                            const float2 ha = make_float2(h0[jj].x, h0[jj].y);
-                            const float2 hb = make_float2(h0[jj].z, h0[jj].w);
-                            const float2 hc = make_float2(h1[jj].x, h1[jj].y);
-                            const float2 hd = make_float2(h1[jj].z, h1[jj].w);
-#pragma unroll
-                            for (int q = 0; q < kDnRows; ++q) {
-                                const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
-                                acc[q][r] = ffma2(bf2(wv.x), ha, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv.y), hb, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv.z), hc, acc[q][r]);
-                                acc[q][r] = ffma2(bf2(wv.w), hd, acc[q][r]);
-                            }
-                        }
-                    }
-                }
-            }
-        }
-    } else {
-        const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
-        for (int bb = lane; bb < I / 16; bb += 32) {
-            // the block's 16 h values of each token, loaded once for all rows
-            float4 hv[NG][4];
-#pragma unroll
-            for (int r = 0; r < NG; ++r) {
-                if (NG <= 2 || r < nr) {
-                    const float4 *hp = reinterpret_cast<const float4 *>(hg + (size_t)r * I + bb * 16);
-#pragma unroll
-                    for (int h4 = 0; h4 < 4; ++h4) hv[r][h4] = __ldcg(hp + h4);
-                }
-            }
-#pragma unroll
-            for (int q = 0; q < kDnRows; ++q) {
-                float2 wf[8];
-                fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
-                const float sc = e4m3f(sb[q * (I / 16) + bb]);
-#pragma unroll
-                for (int r = 0; r < NG; ++r) {
-                    if (NG <= 2 || r < nr) {
-                        float2 p = make_float2(0.f, 0.f);
-#pragma unroll
-                        for (int h4 = 0; h4 < 4; ++h4) {
-                            p = ffma2(wf[2 * h4], make_float2(hv[r][h4].x, hv[r][h4].y), p);
-                            p = ffma2(wf[2 * h4 + 1], make_float2(hv[r][h4].z, hv[r][h4].w), p);
-                        }
-                        acc[q][r].x = fmaf(p.x + p.y, sc, acc[q][r].x);
-                    }
-                }
-            }
-        }
-    }
-    if (nr == 1) {
-        store_four_rows(acc[0][0].x + acc[0][0].y, acc[1][0].x + acc[1][0].y,
-                        acc[2][0].x + acc[2][0].y, acc[3][0].x + acc[3][0].y,
-                        yg, gsc);
-    } else {
-#pragma unroll
-        for (int q = 0; q < kDnRows; ++q) {
-            float yv = 0.f;
-#pragma unroll
-            for (int r = 0; r < NG; ++r) {
-                if (NG <= 2 || r < nr) {
-                    const float sum = warp_sum(acc[q][r].x + acc[q][r].y);
-                    if (lane == r) yv = sum * gsc;
-                }
-            }
-            if (lane < nr) yg[(size_t)lane * d + q] = yv;
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// the kernel
-// ---------------------------------------------------------------------------
-template <int TM, bool FP4>
-__global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kernel(Args a) {
-    constexpr int kThreads = Warps<TM, FP4>::kThreads;
-    constexpr int kConsumers = Warps<TM, FP4>::kConsumers;
-    constexpr int kProducerWarp = Warps<TM, FP4>::kProducerWarp;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int d = a.d, I = a.I, E = a.E, k = a.k, T = a.T, NS = a.nslots, C = a.ncons;
-    const int G = gridDim.x, b = blockIdx.x;
-    uint32_t *err = &a.ws.ctrl->err;
-    Control *ctrl = a.ws.ctrl;
-
-    // ---- shared-memory layout ----
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem);
-    uint64_t *empty = full + kMaxSlots;
-    uint64_t *xbar = empty + kMaxSlots;             // bytes [512, 520)
-    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + 520);
-    int *n_uniq_s = reinterpret_cast<int *>(smem + 524);
-    int *cb_rows_s = reinterpret_cast<int *>(smem + 528);   // [32]
-    int *cb_todo = cb_rows_s + 32;                  // [32]
-    int *n_todo = cb_todo + 32;
-    float *xscale = reinterpret_cast<float *>(smem + 800);  // [16] NVFP4: per-token max|x|
-    float *part = reinterpret_cast<float *>(smem + 1024);   // [8 warps][TM] router partials
-    unsigned char *rbase = smem + 2048;             // routing scratch (8 KB)
-    Route R;
-    R.cnt = reinterpret_cast<int32_t *>(rbase);     // [257]
-    R.off = R.cnt + 260;                            // [257]
-    R.uniq = R.off + 260;                           // [256]
-    R.scan = R.uniq + 260;                          // [257]
-    R.bm = reinterpret_cast<uint32_t *>(R.scan + 260);      // [256]
-    R.ids = reinterpret_cast<int32_t *>(R.bm + 256);        // [16 * 8]
-    R.pos = R.ids + 128;                            // [16 * 8]
-    R.perm = R.pos + 128;                           // [16 * 8]
-    R.w = reinterpret_cast<float *>(R.perm + 128);  // [16 * 8]
-    R.n_uniq = n_uniq_s;
-    unsigned char *xs = smem + 2048 + 8192;
-    const uint32_t x_bytes = a.x_in_smem ? (uint32_t)T * d * 2 : 0u;
-    unsigned char *ring = xs + ((x_bytes + 127) / 128) * 128;
-    // the router's copy of the tokens: the persistent one, or, before the
-    // weight stream starts, the ring
-    const uint32_t xr_bytes = (a.x_in_smem || a.x_router_ring) ? (uint32_t)T * d * 2 : 0u;
-    const unsigned char *xr = a.x_in_smem ? xs : ring;
-
-    if (tid == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(xbar, 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    for (int i = tid; i < 32; i += kThreads) cb_rows_s[i] = 0;
-    __syncthreads();
-    if (tid == 32 * kProducerWarp && xr_bytes) {
-        mbar_arrive_expect_tx(xbar, xr_bytes);
-        bulk_g2s(const_cast<unsigned char *>(xr), a.x, xr_bytes, xbar, policy_evict_last());
-    }
-
-    // ---- 1. router: logits of this CTA's experts ----
-    // experts b, b + G, b + 2G, ... two at a time: warps 0-3 / 4-7 take the
-    // four quarters of one expert's row
-    {
-        const int nq = d / 32;  // 16-byte vectors per quarter row (<= 256: at most 8 per lane)
-        bool x_ready = xr_bytes == 0;
-        for (int base = b; base < E; base += 2 * G) {
-            const int eidx = base + (warp >= 4 ? G : 0);
-            const int q = warp & 3;
-            float acc[TM];
-#pragma unroll
-            for (int t = 0; t < TM; ++t) acc[t] = 0.f;
-            // the router rows are requested before waiting for the tokens' copy
-            uint4 wpre[8];
-            const bool mine = warp < 8 && eidx < E;
-            const uint4 *wrow = reinterpret_cast<const uint4 *>(a.wr + (size_t)eidx * d) + q * nq;
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const int v = lane + 32 * j;
-                wpre[j] = (mine && v < nq) ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
-            }
-            if (!x_ready) {
-                mbar_wait_or_abort(xbar, 0, err, abort_flag);  // a timeout unwinds at the grid barrier below
-                x_ready = true;
-            }
-            if (mine) {
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const int v = lane + 32 * j;
-                    if (v >= nq) continue;
-                    const uint4 wv = wpre[j];
-#pragma unroll
-                    for (int t = 0; t < TM; ++t) {
-                        if (t < T) {
-                            const uint4 xv = xr_bytes
-                                                 ? reinterpret_cast<const uint4 *>(xr + (size_t)t * d * 2)[q * nq + v]
-                                                 : __ldg(reinterpret_cast<const uint4 *>(a.x + (size_t)t * d) + q * nq + v);
-                            float2 s2 = make_float2(0.f, 0.f);
-                            s2 = ffma2(bf2(wv.x), bf2(xv.x), s2);
-                            s2 = ffma2(bf2(wv.y), bf2(xv.y), s2);
-                            s2 = ffma2(bf2(wv.z), bf2(xv.z), s2);
-                            s2 = ffma2(bf2(wv.w), bf2(xv.w), s2);
-                            acc[t] += s2.x + s2.y;
-                        }
-                    }
-                }
-            }
-#pragma unroll
-            for (int t = 0; t < TM; ++t) {
-                const float s = warp_sum(acc[t]);
-                if (lane == 0 && warp < 8) part[warp * TM + t] = s;
-            }
-            __syncthreads();
-            if (tid < 2 * TM) {
-                const int half = tid / TM, t = tid % TM;
-                const int e2 = base + half * G;
-                if (e2 < E && t < T) {
-                    const float *pp = part + half * 4 * TM;
-                    float l = ((pp[0 * TM + t] + pp[1 * TM + t]) + pp[2 * TM + t]) + pp[3 * TM + t];
-                    if (a.bias) l += a.bias[e2];
-                    a.ws.logits[(size_t)t * E + e2] = l;
-                }
-            }
-            __syncthreads();
-        }
-        if (!x_ready) mbar_wait_or_abort(xbar, 0, err, abort_flag);  // CTAs without router rows
-    }
-    grid_barrier(&ctrl->grid_bar.v, (uint32_t)G, err, abort_flag);
-
-    if (FP4 && x_bytes) {
-        // NVFP4 gate/up sums in fp16: keep the staged tokens as fp16(x / max|x|)
-        for (int t = warp; t < T; t += kConsumers + 1) {
-            const uint32_t *xw = reinterpret_cast<const uint32_t *>(xs + (size_t)t * d * 2);
-            float m = 0.f;
-            for (int i = lane; i < d / 2; i += 32) {
-                const uint32_t wv = xw[i];
-                m = fmaxf(m, fmaxf(fabsf(bf16lo(wv)), fabsf(bf16hi(wv))));
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
-            if (lane == 0) xscale[t] = m > 0.f ? m : 1.f;
-        }
-        __syncthreads();
-        for (int i = tid; i < T * (d / 2); i += kThreads) {
-            const float inv = 1.f / xscale[i / (d / 2)];
-            uint32_t *xw = reinterpret_cast<uint32_t *>(xs) + i;
-            const uint32_t wv = *xw;
-            const __half2 hv = __floats2half2_rn(bf16lo(wv) * inv, bf16hi(wv) * inv);
-            *xw = *reinterpret_cast<const uint32_t *>(&hv);
-        }
-        __syncthreads();
-    }
-
-    // ---- 2. routing, computed by every CTA in shared memory ----
-    for (int t = warp; t < T; t += kConsumers + 1)
-        topk_warp(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k, true);
-    if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
-    if (warp == 0 && T == 1) {
-        // one token: its k distinct experts, ascending, are the k rows
-        __syncwarp();
-        const int my = lane < k ? R.ids[lane] : 0x7FFFFFFF;
-        int rank = 0;
-        int cnt_i[8], off_i[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cnt_i[i] = off_i[i] = 0;
-        for (int q = 0; q < k; ++q) {
-            const int o = __shfl_sync(0xFFFFFFFFu, my, q);
-            rank += o < my;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                cnt_i[i] += o == e;
-                off_i[i] += o < e;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) {
-                R.cnt[e] = cnt_i[i];
-                R.off[e] = off_i[i];
-            }
-        }
-        if (lane < k) {
-            R.uniq[rank] = my;
-            R.perm[rank] = 0;
-            R.pos[lane] = rank;
-        }
-        if (lane == 0) {
-            R.off[E] = k;
-            *R.n_uniq = k;
-        }
-    } else if (warp == 0) {
-        // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
-        // tokens ascending within an expert
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) R.bm[e] = 0u;
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
-            if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
-        }
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) {
-            const int c = __popc(R.bm[e]);
-            R.cnt[e] = c;
-            R.scan[e] = c > 0;
-        }
-        __syncwarp();
-        const int total = warp_scan256(R.cnt, R.off, E);
-        __syncwarp();
-        const int nu = warp_scan256(R.scan, R.scan, E);
-        __syncwarp();
-        for (int e = lane; e < E; e += 32)
-            if (R.cnt[e] > 0) R.uniq[R.scan[e]] = e;
-        if (lane == 0) {
-            R.off[E] = total;
-            *R.n_uniq = nu;
-        }
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
-            const int t = p / k;
-            const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
-            R.perm[row] = t;
-            R.pos[p] = row;
-        }
-    }
-    __syncthreads();
-    const int n_uniq = *R.n_uniq;
-    if (b == 0) {  // publish the routing records
-        for (int p = tid; p < T * k; p += kThreads) {
-            a.ws.ids[p] = R.ids[p];
-            a.ws.w[p] = R.w[p];
-            a.ws.pos[p] = R.pos[p];
-            a.ws.perm[p] = R.perm[p];
-        }
-        for (int e = tid; e < E; e += kThreads) {
-            a.ws.counts[e] = R.cnt[e];
-            a.ws.offsets[e] = R.off[e];
-            a.ws.tile_off[e] = 0;
-        }
-        for (int u = tid; u < n_uniq; u += kThreads) a.ws.uniq[u] = R.uniq[u];
-        if (tid == 0) {
-            a.ws.offsets[E] = R.off[E];
-            a.ws.tile_off[E] = 0;
-            ctrl->n_uniq = n_uniq;
-        }
-    }
-
-    // ---- 3./4. the weight stream ----
-    // The active experts are split in two halves, H1 = the first ceil(U/2).
-    // Every CTA streams its share of, in order: H1 gate/up rows, H2 gate/up
-    // rows, H1 down rows, H2 down rows. Down rows of a half wait for that
-    // half's h (a global row count), which the other CTAs finished a whole
-    // segment earlier, so the stream does not stop between the two
-    // projections. A wait only ever sits at a down stage, and every stage that
-    // feeds the counts comes earlier in every CTA's order, so the waits end.
-    // One token: every expert costs the same, equal shares. More: experts
-    // with more tokens cost more per stage; the shares are cut by weight.
-    Plan pl;
-    if (T == 1) {
-        pl = make_plan(n_uniq, I, d / kDnRows, b, G);
-    } else {
-        int32_t *cw = R.scan;  // free after the permutation
-        int32_t *wt = reinterpret_cast<int32_t *>(R.bm);
-        if (warp == 0) {
-            for (int u = lane; u < n_uniq; u += 32) wt[u] = stage_weight(min(R.cnt[R.uniq[u]], TM));
-            __syncwarp();
-            const int total = warp_scan256(wt, cw, n_uniq);
-            if (lane == 0) cw[n_uniq] = total;
-        }
-        __syncthreads();
-        pl = make_plan_weighted(cw, n_uniq, I, d / kDnRows, b, G);
-    }
-    const int n_gu = pl.nA + pl.nB;
-    const int n_st = n_gu + pl.nC + pl.nD;
-    const int U1 = (n_uniq + 1) / 2;
-    const uint32_t rbg = rowb<FP4>(d), rbd = rowb<FP4>(I);
-
-    if (warp == kProducerWarp) {
-        // a.nprod lanes fill the ring, lane l the slots j with j % nprod == l
-        // (nslots is a multiple of nprod), so every slot's fills come from one
-        // lane in order. The lanes poll their next slot without blocking and
-        // stay converged: a lane that sleeps in a blocking wait holds up the
-        // other lanes of its warp, whose slots may long be free.
-        const int P = a.nprod;
-        const uint64_t pol = policy_evict_first();
-        int s = lane;
-        unsigned long long t_progress = global_ns();
-        for (uint32_t it = 1;; ++it) {
-            const bool live = lane < P && s < n_st;
-            if (!__any_sync(0xFFFFFFFFu, live)) break;
-            const int slot = s % NS;
-            const bool ready = live && (s < NS || mbar_test_wait(&empty[slot], ((s / NS) - 1) & 1));
-            if (ready) {
-                unsigned char *dst = ring + (size_t)slot * a.slot_bytes;
-                if (s < n_gu) {
-                    const int g = pl.gu_row(s);
-                    const int u = g / I, i = g - u * I;
-                    const size_t row = (size_t)R.uniq[u] * I + i;
-                    mbar_arrive_expect_tx(&full[slot], 2 * rbg);
-                    if (!FP4) {
-                        bulk_g2s(dst, a.wg + row * d, rbg, &full[slot], pol);
-                        bulk_g2s(dst + rbg, a.wu + row * d, rbg, &full[slot], pol);
-                    } else {
-                        const uint32_t nq = d / 2, nsb = d / 16;
-                        bulk_g2s(dst, a.qg + row * nq, nq, &full[slot], pol);
-                        bulk_g2s(dst + nq, a.sg + row * nsb, nsb, &full[slot], pol);
-                        bulk_g2s(dst + rbg, a.qu + row * nq, nq, &full[slot], pol);
-                        bulk_g2s(dst + rbg + nq, a.su + row * nsb, nsb, &full[slot], pol);
-                    }
-                } else {
-                    const int g = pl.dn_unit(s - n_gu) * kDnRows;
-                    const int u = g / d, c0 = g - u * d;
-                    const size_t row = (size_t)R.uniq[u] * d + c0;
-                    mbar_arrive_expect_tx(&full[slot], kDnRows * rbd);
-                    if (!FP4) {
-                        bulk_g2s(dst, a.wd + row * I, kDnRows * rbd, &full[slot], pol);
-                    } else {
-                        const uint32_t nq = I / 2, nsb = I / 16;
-                        bulk_g2s(dst, a.qd + row * nq, kDnRows * nq, &full[slot], pol);
-                        bulk_g2s(dst + kDnRows * nq, a.sd + row * nsb, kDnRows * nsb, &full[slot], pol);
-                    }
-                }
-                s += P;
-            }
-            // bounded: give up once no lane has issued for the wait limit
-            if (__any_sync(0xFFFFFFFFu, ready)) {
-                t_progress = 0;
-            } else if ((it & 255u) == 0) {
-                const unsigned long long now = global_ns();
-                if (t_progress == 0) t_progress = now;
-                const bool other_gave_up = *abort_flag != 0;
-                const bool timed_out = now - t_progress > kWaitLimitNs;
-                if (__any_sync(0xFFFFFFFFu, other_gave_up || timed_out)) {  // the whole warp leaves together
-                    if (lane == 0 && !other_gave_up) {
-                        atomicOr(err, ERRBIT_TIMEOUT);
-                        *abort_flag = 1;
-                    }
-                    break;
-                }
-            }
-        }
-        __syncwarp();
-        // every copy this lane issued must land before the CTA moves on (in a
-        // normal run the consumers have waited for all of them already)
-        if (lane < P) {
-            // the lane's last fill of each of its slots: stages s - NS .. s - P
-            // (s and NS - P are multiples of P apart from lane)
-            for (int j = max(lane, s - NS); j < s; j += P) mbar_wait(&full[j % NS], (j / NS) & 1, err);
-        }
-    } else if (warp < C) {
-        // ------------------------------- gate/up -------------------------------
-        Seg<TM> seg;
-        int s = warp;
-        int done_a = 0, done_b = 0;   // this warp's finished h rows of each half
-        bool pub_a = false;
-        for (; s < n_gu && !*abort_flag; s += C) {
-            if (s >= pl.nA && !pub_a) {
-                publish_rows(&ctrl->h_ready[0].v, done_a);
-                pub_a = true;
-            }
-            if (s < pl.nA)
-                ++done_a;
-            else
-                ++done_b;
-            const int slot = s % NS;
-            const int g = pl.gu_row(s);
-            const int u = g / I, i = g - u * I;
-            if (u != seg.u) seg_load(seg, R, u);
-            if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
-            const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
-            if (TM == 1 || seg.n_e == 1)
-                gu_stage<1, TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
-            else if (TM == 2 || seg.n_e == 2)
-                gu_stage<(TM < 2 ? TM : 2), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
-            else if (TM == 4 || seg.n_e <= 4)
-                gu_stage<(TM < 4 ? TM : 4), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
-            else if (TM == 8 || seg.n_e <= 8)
-                gu_stage<(TM < 8 ? TM : 8), TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
-            else
-                gu_stage<TM, TM, FP4>(a, st, xs, xscale, seg, &empty[slot], i);
-        }
-        // this warp's h rows are written: count them in
-        if (!pub_a) publish_rows(&ctrl->h_ready[0].v, done_a);
-        publish_rows(&ctrl->h_ready[1].v, done_b);
-        bool ready_a = false, ready_b = false;
-        // ---------------------------------- down ----------------------------------
-        Seg<TM> sd;
-        // an expert with one token: its h row stays in registers for all the
-        // warp's stages of that expert (I <= 2048)
-        constexpr int kHC = 8;
-        float4 hc0[kHC], hc1[kHC];
-        int hc_u = -1;
-        for (; s < n_st && !*abort_flag; s += C) {
-            const int t = s - n_gu;
-            if (t < pl.nC && !ready_a) {
-                if (!wait_rows(&ctrl->h_ready[0].v, (uint32_t)(U1 * I), err, abort_flag)) break;
-                ready_a = true;
-            }
-            if (t >= pl.nC && !ready_b) {
-                if (!wait_rows(&ctrl->h_ready[1].v, (uint32_t)((n_uniq - U1) * I), err, abort_flag)) break;
-                ready_b = true;
-            }
-            const int slot = s % NS;
-            const int g = pl.dn_unit(t) * kDnRows;
-            const int u = g / d, c0 = g - u * d;
-            if (u != sd.u) seg_load(sd, R, u);
-            if (!mbar_wait_or_abort(&full[slot], (s / NS) & 1, err, abort_flag)) break;
-            const unsigned char *st = ring + (size_t)slot * a.slot_bytes;
-            const float *hrow = a.ws.h + (size_t)sd.row0 * I;
-            const float gsc = FP4 ? a.gd[sd.e] : 1.f;
-            const int nvec = I / 8;
-            if (!FP4 && sd.n_e == 1 && nvec <= 32 * kHC) {
-                // one token, its h row held in registers across the expert's stages
-                if (hc_u != sd.u) {
-                    const float4 *hr = reinterpret_cast<const float4 *>(hrow);
-#pragma unroll
-                    for (int jj = 0; jj < kHC; ++jj) {
-                        const int v = lane + 32 * jj;
-                        if (v < nvec) {
-                            hc0[jj] = __ldcg(hr + 2 * v);
-                            hc1[jj] = __ldcg(hr + 2 * v + 1);
-                        }
-                    }
-                    hc_u = sd.u;
-                }
-                float2 acc[kDnRows];
-#pragma unroll
-                for (int q = 0; q < kDnRows; ++q) acc[q] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int jj = 0; jj < kHC; ++jj) {
-                    const int v = lane + 32 * jj;
-                    if (v < nvec) {
-                        const float2 ha = make_float2(hc0[jj].x, hc0[jj].y), hb = make_float2(hc0[jj].z, hc0[jj].w);
-                        const float2 hc = make_float2(hc1[jj].x, hc1[jj].y), hd = make_float2(hc1[jj].z, hc1[jj].w);
-#pragma unroll
-                        for (int q = 0; q < kDnRows; ++q) {
-                            const uint4 wv = reinterpret_cast<const uint4 *>(st + q * rbd)[v];
-                            acc[q] = ffma2(bf2(wv.x), ha, acc[q]);
-                            acc[q] = ffma2(bf2(wv.y), hb, acc[q]);
-                            acc[q] = ffma2(bf2(wv.z), hc, acc[q]);
-                            acc[q] = ffma2(bf2(wv.w), hd, acc[q]);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-                store_four_rows(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y, acc[3].x + acc[3].y,
-                                a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
-            } else if (FP4 && sd.n_e == 1 && I / 16 <= 32 * (kHC / 2)) {
-                // NVFP4, one token: lane block j (16 elements of h) held in
-                // hc0[2j], hc0[2j+1], hc1[2j], hc1[2j+1] across the expert's stages
-                if (hc_u != sd.u) {
-#pragma unroll
-                    for (int j = 0; j < kHC / 2; ++j) {
-                        const int bb = lane + 32 * j;
-                        if (bb < I / 16) {
-                            const float4 *hp = reinterpret_cast<const float4 *>(hrow + bb * 16);
-                            hc0[2 * j] = __ldcg(hp);
-                            hc0[2 * j + 1] = __ldcg(hp + 1);
-                            hc1[2 * j] = __ldcg(hp + 2);
-                            hc1[2 * j + 1] = __ldcg(hp + 3);
-                        }
-                    }
-                    hc_u = sd.u;
-                }
-                const unsigned char *qb = st, *sb = st + kDnRows * (I / 2);
-                float acc[kDnRows];
-#pragma unroll
-                for (int q = 0; q < kDnRows; ++q) acc[q] = 0.f;
-#pragma unroll
-                for (int j = 0; j < kHC / 2; ++j) {
-                    const int bb = lane + 32 * j;
-                    if (bb < I / 16) {
-                        const float4 h0 = hc0[2 * j], h1 = hc0[2 * j + 1], h2 = hc1[2 * j], h3 = hc1[2 * j + 1];
-#pragma unroll
-                        for (int q = 0; q < kDnRows; ++q) {
-                            float2 wf[8];
-                            fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
-                            const float sc = e4m3f(sb[q * (I / 16) + bb]);
-                            float2 p = make_float2(0.f, 0.f), p1 = make_float2(0.f, 0.f);
-                            p = ffma2(wf[0], make_float2(h0.x, h0.y), p);
-                            p1 = ffma2(wf[1], make_float2(h0.z, h0.w), p1);
-                            p = ffma2(wf[2], make_float2(h1.x, h1.y), p);
-                            p1 = ffma2(wf[3], make_float2(h1.z, h1.w), p1);
-                            p = ffma2(wf[4], make_float2(h2.x, h2.y), p);
-                            p1 = ffma2(wf[5], make_float2(h2.z, h2.w), p1);
-                            p = ffma2(wf[6], make_float2(h3.x, h3.y), p);
-                            p1 = ffma2(wf[7], make_float2(h3.z, h3.w), p1);
-                            acc[q] = fmaf((p.x + p1.x) + (p.y + p1.y), sc, acc[q]);
-                        }
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-                store_four_rows(acc[0], acc[1], acc[2], acc[3], a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
-            } else {
-                // the expert's tokens in groups of up to TG (bounded registers)
-                constexpr int TG = TM < 4 ? TM : 4;
-                for (int r0 = 0; r0 < sd.n_e; r0 += TG) {
-                    const int nr = min(TG, sd.n_e - r0);
-                    const float *hg = hrow + (size_t)r0 * I;
-                    float *yg = a.ws.Y + (size_t)(sd.row0 + r0) * d + c0;
-                    if (nr == 1)
-                        dn_group<1, FP4>(a, st, hg, 1, yg, gsc);
-                    else if (nr == 2)
-                        dn_group<(TG < 2 ? TG : 2), FP4>(a, st, hg, nr, yg, gsc);
-                    else if (nr <= 4)
-                        dn_group<(TG < 4 ? TG : 4), FP4>(a, st, hg, nr, yg, gsc);
-                    else
-                        dn_group<TG, FP4>(a, st, hg, nr, yg, gsc);
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&empty[slot]);
-            }
-            if (lane == 0) atomicAdd(&cb_rows_s[c0 / kCb], kDnRows);
-        }
-    }
-
-    // ---- 5. combine, by the CTA that completes each column block ----
-    fence_acq_rel_gpu();  // this thread's h and Y stores before the block's count below
-    __syncthreads();
-    if (a.do_combine) {
-        if (warp == 0) {
-            // lane cb counts this CTA's rows of column block cb in; the
-            // counts go out together rather than one round trip after another
-            const int ncb = (d + kCb - 1) / kCb;
-            bool fin = false;
-            fence_acq_rel_gpu();  // the CTA's stores (ordered by the barrier) before this lane's count
-            if (lane < ncb) {
-                const int mine = cb_rows_s[lane];
-                if (mine) {
-                    const int cols = min(kCb, d - lane * kCb);
-                    const uint32_t done = atomicAdd(&ctrl->cb_rows[lane].v, (uint32_t)mine) + mine;
-                    fin = done == (uint32_t)(n_uniq * cols);
-                }
-            }
-            fence_acq_rel_gpu();
-            const uint32_t fin_mask = __ballot_sync(0xFFFFFFFFu, fin);
-            if (lane == 0) {
-                int n = 0;
-                for (uint32_t m = fin_mask; m; m &= m - 1) cb_todo[n++] = __ffs(m) - 1;
-                *n_todo = n;
-            }
-        }
-        __syncthreads();
-        for (int ti = 0; ti < *n_todo; ++ti) {
-            const int cb = cb_todo[ti];
-            const int cols = min(kCb, d - cb * kCb);
-            for (int idx = tid; idx < T * (cols / 4); idx += kThreads) {
-                const int t = idx / (cols / 4);
-                const int c = cb * kCb + (idx % (cols / 4)) * 4;
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-                for (int j = 0; j < k; ++j) {
-                    const float wj = R.w[t * k + j];
-                    const float4 y = __ldcg(reinterpret_cast<const float4 *>(a.ws.Y + (size_t)R.pos[t * k + j] * d + c));
-                    acc.x = fmaf(wj, y.x, acc.x);
-                    acc.y = fmaf(wj, y.y, acc.y);
-                    acc.z = fmaf(wj, y.z, acc.z);
-                    acc.w = fmaf(wj, y.w, acc.w);
-                }
-                if (a.res) {
-                    const uint2 rv = *reinterpret_cast<const uint2 *>(a.res + (size_t)t * d + c);
-                    acc.x += bf16lo(rv.x);
-                    acc.y += bf16hi(rv.x);
-                    acc.z += bf16lo(rv.y);
-                    acc.w += bf16hi(rv.y);
-                }
-                uint2 o;
-                o.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
-                o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
-                *reinterpret_cast<uint2 *>(a.out + (size_t)t * d + c) = o;
-            }
-            if (tid == 0) ctrl->cb_rows[cb].v = 0u;
-        }
-    }
-    // ---- exit: the last CTA out resets the grid-barrier counters ----
-    __syncthreads();
-    if (tid == 0) {
-        fence_acq_rel_gpu();
-        if (atomicAdd(&ctrl->grid_exit.v, 1u) == (uint32_t)G - 1) {
-            for (int cb = 0; cb < 32; ++cb) ctrl->cb_rows[cb].v = 0u;  // zero already unless a wait gave up
-            ctrl->grid_bar.v = 0u;
-            ctrl->h_ready[0].v = 0u;
-            ctrl->h_ready[1].v = 0u;
-            ctrl->grid_exit.v = 0u;
-            fence_acq_rel_gpu();
-        }
-    }
-}
-
-template <int TM, bool FP4>
-static int pick(int fit, int &ncons) {
-    if (fit > kMaxSlots) fit = kMaxSlots;
-    for (int c = Warps<TM, FP4>::kConsumers; c >= 1; --c)
-        if (fit / c >= 2) {
-            ncons = c;
-            return (fit / c) * c;
-        }
-    ncons = 1;
-    return fit;
-}
-
-template <int TM, bool FP4>
-static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16_t *x, const uint16_t *res,
-                            uint16_t *out, int T, cudaStream_t st) {
-    Args a{};
-    a.x = x;
-    a.res = res;
-    a.out = out;
-    a.wr = L.wr;
-    a.bias = L.bias;
-    a.wg = L.wg;
-    a.wu = L.wu;
-    a.wd = L.wd;
-    a.qg = L.qg;
-    a.qu = L.qu;
-    a.qd = L.qd;
-    a.sg = L.sg;
-    a.su = L.su;
-    a.sd = L.sd;
-    a.gg = L.gg;
-    a.gu = L.gu;
-    a.gd = L.gd;
-    a.T = T;
-    a.d = L.d;
-    a.I = L.I;
-    a.E = L.E;
-    a.k = L.k;
-    a.ws = ws;
-    a.do_combine = L.expert_norm ? 0 : 1;
-    const uint32_t slot = (uint32_t)(2 * rowb<FP4>(L.d) > kDnRows * rowb<FP4>(L.I) ? 2 * rowb<FP4>(L.d)
-                                                                                     : kDnRows * rowb<FP4>(L.I));
-    a.slot_bytes = (slot + 127) / 128 * 128;
-    const size_t fixed = 2048 + 8192;
-    a.x_in_smem = T <= 8 ? 1 : 0;
-    const size_t xb = a.x_in_smem ? align_up((size_t)T * L.d * 2, 128) : 0;
-    if (fixed + xb + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) {
-        a.x_in_smem = 0;
-    }
-    const size_t xb2 = a.x_in_smem ? xb : 0;
-    if (fixed + xb2 + 2 * (size_t)a.slot_bytes > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
-    const int fit = (int)((kSmemBudget - fixed - xb2) / a.slot_bytes);
-    a.nslots = pick<TM, FP4>(fit, a.ncons);
-    a.x_router_ring = !a.x_in_smem && (size_t)a.nslots * a.slot_bytes >= (size_t)T * L.d * 2 ? 1 : 0;
-    a.nprod = a.nslots % 4 == 0 ? 4 : (a.nslots % 2 == 0 ? 2 : 1);
-    const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<TM, FP4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(L.num_sms);
-    cfg.blockDim = dim3(Warps<TM, FP4>::kThreads);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attrs[1];
-    attrs[0].id = cudaLaunchAttributeCooperative;
-    attrs[0].val.cooperative = 1;
-    cfg.attrs = attrs;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, decode_layer_kernel<TM, FP4>, a);
-}
-
-}  // namespace fused
 
 // Whole small-batch layer in one launch (plus the normalising combine when
 // the layer asks for per-expert output normalisation).
@@ -1273,7 +12,7 @@ cudaError_t launch_decode_fused(const LayerDev &L, const Workspace &ws, const ui
     if (L.E > 256 || L.k > 8 || T > 16 || L.d > 32 * kCb) return cudaErrorInvalidValue;
     cudaError_t e;
     const bool fp4 = L.fmt == MOE_W_NVFP4;
-#define MOE_FUSED(TMV) e = fp4 ? launch_t<TMV, true>(L, ws, x, res, out, T, st) : launch_t<TMV, false>(L, ws, x, res, out, T, st)
+#define MOE_FUSED(TMV) e = fp4 ? launch_t<TMV, true, false>(L, ws, x, res, out, T, st) : launch_t<TMV, false, false>(L, ws, x, res, out, T, st)
     if (T <= 1)
         MOE_FUSED(1);
     else if (T <= 2)
