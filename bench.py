@@ -95,11 +95,13 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.22e6 + 3.80e6,
-                  "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cu",
+    "decode_t1": {"bytes": 304.22e6 + 3.41e6,
+                  "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
+                              "top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh"),
-                  "sha256": ("8011892625a1d9359ba7a1546b661093603cdf23dbfbd1a0f1388227e7e55e8e",
-                             "86673bf78aa13ea87d52b2615158509ccddf2d2c723433109c951e2f7724e4c0")},
+                  "sha256": ("ea55e698e0460adf6381a67d76183d6a086e04a0caa62de811821abd197840f9",
+                             "1d39e048978fb78a6191116a4ce545b150e1efd7577999126a1f97db51c5e355",
+                             "51bf09099eb479424d60cbb99e4838e2b5c30817818ab33fdb8c84adf604c2ac")},
 }
 
 
