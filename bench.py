@@ -99,9 +99,9 @@ TRAFFIC = {
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh"),
-                  "sha256": ("ea55e698e0460adf6381a67d76183d6a086e04a0caa62de811821abd197840f9",
+                  "sha256": ("2c643950cd952119773070b980c2ff448738d8017fb2fbd33a5a4b44c01442d8",
                              "1d39e048978fb78a6191116a4ce545b150e1efd7577999126a1f97db51c5e355",
-                             "51bf09099eb479424d60cbb99e4838e2b5c30817818ab33fdb8c84adf604c2ac")},
+                             "7dd70629dc137bc914f03f15ee8566d22afb9a3e9583266dc02b5c21e57e759f")},
 }
 
 

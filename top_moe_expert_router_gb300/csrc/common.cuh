@@ -46,8 +46,8 @@ struct Control {
 constexpr int kRouteChunk = 32;
 
 // The large-batch router GEMM splits K (= d) in up to kRouterSplit parts, each
-// written to its own slice of the logits region; the top-k sums the parts in
-// order. d is a multiple of 64 (the GEMM's K block).
+// written to its own slice of the logits region; the large-batch top-k sums
+// the parts in order. d is a multiple of 64 (the GEMM's K block).
 constexpr int kRouterSplit = 4;
 inline int router_ksplit(int d) {
     const int kb = d / 64;
@@ -155,23 +155,15 @@ __device__ __forceinline__ float key_value(uint32_t key) {
 // the kept, summed in pick order. Lane l holds experts l, l + 32, ...; each
 // pick is a warp-wide max of the lanes' best keys and a warp-wide min of the
 // ids that reach it. bypass_l1: read the logits through L2 only (they were
-// written by other CTAs of the same launch). nsplit > 1: the logit is the sum,
-// in order, of nsplit parts split_stride floats apart.
+// written by other CTAs of the same launch).
 __device__ __forceinline__ void topk_warp(const float *logits_row, int E, int k, int32_t *ids_out, float *w_out,
-                                          bool bypass_l1, int nsplit = 1, size_t split_stride = 0) {
+                                          bool bypass_l1) {
     const int lane = threadIdx.x & 31;
     uint32_t key[8];
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int e = lane + 32 * i;
-        float l = 0.f;
-        if (e < E) {
-            // the logit's parts over K, added in order
-            l = bypass_l1 ? __ldcg(logits_row + e) : logits_row[e];
-            for (int s = 1; s < nsplit; ++s)
-                l += bypass_l1 ? __ldcg(logits_row + s * split_stride + e) : logits_row[s * split_stride + e];
-        }
-        key[i] = e < E ? order_key(l) : 0u;
+        key[i] = e < E ? order_key(bypass_l1 ? __ldcg(logits_row + e) : logits_row[e]) : 0u;
     }
     uint32_t my_key = 0u;
     int my_id = 0;

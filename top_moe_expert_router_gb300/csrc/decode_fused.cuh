@@ -12,10 +12,11 @@
 //   2. routing: every CTA computes top-k and the permutation of all T tokens
 //      itself, in shared memory (identical results everywhere; CTA 0 also
 //      publishes them), so no second barrier is needed;
-//   3. one producer lane fills a ring of shared-memory slots with bulk TMA
-//      copies: first this CTA's share of the active experts' gate/up rows,
-//      then, without a pause, its share of their down rows; slot j belongs
-//      to consumer warp j % c, which takes the slot's phases in order;
+//   3. producer lanes (polling, never blocking) fill a ring of shared-memory
+//      slots with bulk TMA copies: first this CTA's share of the active
+//      experts' gate/up rows, then, without a pause, its share of their down
+//      rows (shares cut by cost when experts carry several tokens); slot j
+//      belongs to consumer warp j % c, which takes the slot's phases in order;
 //   4. consumer warps compute h = silu(Wg x) * (Wu x) (fp32, to global) and
 //      count the rows in, per half of the active experts; the stream runs
 //      first-half gate/up, second-half gate/up, first-half down, second-half
@@ -25,7 +26,9 @@
 //      complete the block (a row counter per block) forms
 //      out = (res +) sum_j w_j Y_j for those columns, in fp32, j ascending.
 // Every wait (mbarrier, grid barrier) is bounded; a timeout sets the error
-// word and the kernel unwinds.
+// word and the kernel unwinds. With STACK the kernel loops over layers
+// (decode_stack.cu): each layer's input is RMSNorm of the previous output,
+// computed in every CTA, and a grid barrier separates the layers.
 #pragma once
 
 #include <cuda_fp4.h>
