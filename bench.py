@@ -95,7 +95,7 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.22e6 + 3.41e6,
+    "decode_t1": {"bytes": 304.22e6 + 3.56e6,
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh"),
