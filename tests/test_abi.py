@@ -77,6 +77,18 @@ def test_calls_reject_null_layer_and_bad_sizes(lib):
     assert moe.status_string(moe.MOE_ERR_TIMEOUT) == "kernel wait timed out"
 
 
+def test_stack_calls_reject_bad_arguments(lib):
+    h = ctypes.c_void_p()
+    assert lib.moe_stack_create(None, 2, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    handles = (ctypes.c_void_p * 2)(None, None)
+    assert lib.moe_stack_create(handles, 0, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_create(handles, 65, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_create(handles, 2, ctypes.byref(h)) == moe.MOE_ERR_INVALID_ARG   # null layers
+    assert lib.moe_stack_forward(None, ctypes.c_void_p(4096), ctypes.c_void_p(8192), 1, 1e-6, None,
+                                 None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_destroy(None) == moe.MOE_OK
+
+
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(OSError):
         ctypes.CDLL(str(tmp_path / "libmoe.so"))
