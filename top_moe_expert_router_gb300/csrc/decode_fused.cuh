@@ -1127,18 +1127,36 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                 store_four_rows(acc[0].x + acc[0].y, acc[1].x + acc[1].y, acc[2].x + acc[2].y, acc[3].x + acc[3].y,
                                 a.ws.Y + (size_t)sd.row0 * d + c0, gsc);
             } else if (FP4 && sd.n_e == 1 && I / 16 <= 32 * (kHC / 2)) {
-                // NVFP4, one token: lane block j (16 elements of h) held in
-                // hc0[2j], hc0[2j+1], hc1[2j], hc1[2j+1] across the expert's stages
+                // NVFP4, one token: lane block j (16 elements of h) held across
+                // the expert's stages as fp16(h / max|h_block|) in hc0[2j],
+                // hc0[2j+1] (eight f16 pairs) with the block's max|h| in
+                // hc1[2j].x; the 16 products of a block (|e2m1| <= 6, |h'| <= 1)
+                // are summed in fp16, then scaled in fp32
                 if (hc_u != sd.u) {
 #pragma unroll
                     for (int j = 0; j < kHC / 2; ++j) {
                         const int bb = lane + 32 * j;
                         if (bb < I / 16) {
                             const float4 *hp = reinterpret_cast<const float4 *>(hrow + bb * 16);
-                            hc0[2 * j] = __ldcg(hp);
-                            hc0[2 * j + 1] = __ldcg(hp + 1);
-                            hc1[2 * j] = __ldcg(hp + 2);
-                            hc1[2 * j + 1] = __ldcg(hp + 3);
+                            const float4 v[4] = {__ldcg(hp), __ldcg(hp + 1), __ldcg(hp + 2), __ldcg(hp + 3)};
+                            float m = 0.f;
+#pragma unroll
+                            for (int r = 0; r < 4; ++r)
+                                m = fmaxf(m, fmaxf(fmaxf(fabsf(v[r].x), fabsf(v[r].y)), fmaxf(fabsf(v[r].z), fabsf(v[r].w))));
+                            const float hs = m > 0.f ? m : 1.f, inv = 1.f / hs;
+                            uint32_t hw[8];
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                const __half2 lo = __floats2half2_rn(v[r].x * inv, v[r].y * inv);
+                                const __half2 hi = __floats2half2_rn(v[r].z * inv, v[r].w * inv);
+                                hw[2 * r] = *reinterpret_cast<const uint32_t *>(&lo);
+                                hw[2 * r + 1] = *reinterpret_cast<const uint32_t *>(&hi);
+                            }
+                            hc0[2 * j] = make_float4(__uint_as_float(hw[0]), __uint_as_float(hw[1]),
+                                                     __uint_as_float(hw[2]), __uint_as_float(hw[3]));
+                            hc0[2 * j + 1] = make_float4(__uint_as_float(hw[4]), __uint_as_float(hw[5]),
+                                                         __uint_as_float(hw[6]), __uint_as_float(hw[7]));
+                            hc1[2 * j].x = hs;
                         }
                     }
                     hc_u = sd.u;
@@ -1151,22 +1169,31 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                 for (int j = 0; j < kHC / 2; ++j) {
                     const int bb = lane + 32 * j;
                     if (bb < I / 16) {
-                        const float4 h0 = hc0[2 * j], h1 = hc0[2 * j + 1], h2 = hc1[2 * j], h3 = hc1[2 * j + 1];
+                        const float4 A = hc0[2 * j], B = hc0[2 * j + 1];
+                        const uint32_t hw[8] = {__float_as_uint(A.x), __float_as_uint(A.y), __float_as_uint(A.z),
+                                                __float_as_uint(A.w), __float_as_uint(B.x), __float_as_uint(B.y),
+                                                __float_as_uint(B.z), __float_as_uint(B.w)};
+                        const __half2 *hh = reinterpret_cast<const __half2 *>(hw);
+                        const float hs = hc1[2 * j].x;
 #pragma unroll
                         for (int q = 0; q < kDnRows; ++q) {
-                            float2 wf[8];
-                            fp4x16(*reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8), wf);
-                            const float sc = e4m3f(sb[q * (I / 16) + bb]);
-                            float2 p = make_float2(0.f, 0.f), p1 = make_float2(0.f, 0.f);
-                            p = ffma2(wf[0], make_float2(h0.x, h0.y), p);
-                            p1 = ffma2(wf[1], make_float2(h0.z, h0.w), p1);
-                            p = ffma2(wf[2], make_float2(h1.x, h1.y), p);
-                            p1 = ffma2(wf[3], make_float2(h1.z, h1.w), p1);
-                            p = ffma2(wf[4], make_float2(h2.x, h2.y), p);
-                            p1 = ffma2(wf[5], make_float2(h2.z, h2.w), p1);
-                            p = ffma2(wf[6], make_float2(h3.x, h3.y), p);
-                            p1 = ffma2(wf[7], make_float2(h3.z, h3.w), p1);
-                            acc[q] = fmaf((p.x + p1.x) + (p.y + p1.y), sc, acc[q]);
+                            const uint2 cq = *reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8);
+                            __half2 wh[8];
+#pragma unroll
+                            for (int m = 0; m < 8; ++m) {
+                                const uint32_t word = m < 4 ? cq.x : cq.y;
+                                __half2_raw r2 = __nv_cvt_fp4x2_to_halfraw2(
+                                    (__nv_fp4x2_storage_t)((word >> (8 * (m & 3))) & 0xFFu), __NV_E2M1);
+                                wh[m] = *reinterpret_cast<__half2 *>(&r2);
+                            }
+                            __half2 p0 = __hmul2(wh[0], hh[0]), p1 = __hmul2(wh[1], hh[1]);
+#pragma unroll
+                            for (int m = 2; m < 8; m += 2) {
+                                p0 = __hfma2(wh[m], hh[m], p0);
+                                p1 = __hfma2(wh[m + 1], hh[m + 1], p1);
+                            }
+                            const float2 f = __half22float2(__hadd2(p0, p1));
+                            acc[q] = fmaf(f.x + f.y, e4m3f(sb[q * (I / 16) + bb]) * hs, acc[q]);
                         }
                     }
                 }
