@@ -95,11 +95,11 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.22e6 + 3.56e6,
+    "decode_t1": {"bytes": 304.22e6 + 3.52e6,
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh"),
-                  "sha256": ("2c643950cd952119773070b980c2ff448738d8017fb2fbd33a5a4b44c01442d8",
+                  "sha256": ("6d828c4220d259f61ae9b2d532b6178dadd6062a79eafbf6cc60c4a174d426cb",
                              "1d39e048978fb78a6191116a4ce545b150e1efd7577999126a1f97db51c5e355",
                              "7dd70629dc137bc914f03f15ee8566d22afb9a3e9583266dc02b5c21e57e759f")},
 }
