@@ -3,28 +3,35 @@
 
 A step is one pass of the whole layer (router, softmax/top-8/renormalise,
 permutation, expert SwiGLU FFNs, weighted combine) over one batch of
-synthetic tokens with the weights resident in HBM. The default workload is
-single-request decode: T=1 token, d=4096, E=256 experts, top-8, I=1536, bf16
-expert weights; tokens rotate through a pool of 64 seeded N(0,1) rows and L2
-is flushed (256 MiB write) before every step, so every step streams its 8
-experts' weights (302 MB) from HBM.
+synthetic tokens, with the weights resident in HBM. The default run measures
+all five workloads of the layer (d=4096, E=256 experts, top-8, I=1536):
 
-    python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME]
+  decode_t1        T=1 single-request decode, bf16 experts      (the headline)
+  decode_t4/_t16   T=4 / 16 batched decode / speculative verify, bf16 experts
+  prefill_t4096    T=4096 prefill, bf16 experts, Zipf-skewed router bias
+  nvfp4_stack_t4   8 stacked layers (RMSNorm, MoE, residual), T=4, NVFP4 experts
 
-Prints one JSON line. Under torchrun (N > 1) every rank holds a full layer
-replica and processes its own tokens (no data-path collective); rank 0
-prints the line, with the time taken as the max over ranks.
+and prints ONE JSON line: the headline's fields at the top level and every
+workload's measurement under "workloads". Tokens rotate through a pool of 64
+seeded N(0,1) batches and L2 is flushed (256 MiB write) before every step,
+outside the step's CUDA events, so every step streams its weights from HBM.
+
+    python bench.py [--gpus N --steps K --warmup W] [--impl reference] [--workload NAME|all]
+
+Under torchrun (N > 1) every rank holds full layer replicas and processes its
+own tokens (no data-path collective); rank 0 prints the line, with each
+workload's time taken as the max over ranks.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import statistics
 import subprocess
 import sys
 import tempfile
-import threading
 import time
 
 import numpy as np
@@ -38,6 +45,8 @@ METRIC = "MoE-layer tok/s; decode HBM GB/s vs ~8 TB/s; prefill TFLOP/s vs bf16 p
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 FLUSH_BYTES = 256 << 20
 POOL = 64
+HEADLINE = "decode_t1"
+ORDER = ["decode_t1", "decode_t4", "decode_t16", "prefill_t4096", "nvfp4_stack_t4"]
 
 
 # ---------------------------------------------------------------------------
@@ -47,12 +56,12 @@ POOL = 64
 def parse_args(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("--gpus", type=int, default=1)
-    p.add_argument("--steps", type=int, default=2000)
-    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--steps", type=int, default=200)
+    p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="decode_t1", choices=sorted(datagen.WORKLOADS))
+    p.add_argument("--workload", default="all", choices=["all"] + ORDER)
     p.add_argument("--no-cpu-baseline", action="store_true")
-    p.add_argument("--e2e-steps", type=int, default=500)
+    p.add_argument("--e2e-steps", type=int, default=200)
     p.add_argument("--experts", type=int, default=0,
                    help="override E (a smaller layer of the same kernels, for profiler captures)")
     return p.parse_args(argv)
@@ -192,53 +201,161 @@ def workload_config(w: datagen.Workload, **extra):
     return cfg
 
 
+def token_pool(w: datagen.Workload, rank: int):
+    """Each rank's POOL batches of w.T tokens (distinct rows of the token stream)."""
+    return [datagen.tokens(w, w.T, start_row=(rank * POOL + i) * w.T) for i in range(POOL)]
+
+
 # ---------------------------------------------------------------------------
-# CPU oracle: the reference arm and the cpu_baseline leg
+# CPU oracle: the reference arm and the cpu_baseline legs
 # ---------------------------------------------------------------------------
 
-def oracle_token_rate(host_layer, x_tokens: np.ndarray, budget_s: float = 20.0):
-    """Oracle throughput (tok/s) on a bounded sample of tokens, all threads."""
-    import oracle
-    n = x_tokens.shape[0]
+def _timed(fn, budget_s: float, max_calls: int):
+    """Calls fn(i) for i = 0, 1, ... until budget_s has passed (at least once,
+    at most max_calls). Returns (calls, seconds)."""
     t0 = time.perf_counter()
-    host_layer.forward(x_tokens)
-    dt = time.perf_counter() - t0
-    return n / dt, dt, oracle.max_threads()
+    n = 0
+    while n < max_calls:
+        fn(n)
+        n += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    return n, time.perf_counter() - t0
+
+
+def oracle_decode_rates(w, wr, bias, pool_np, budget_s=4.0):
+    """Oracle tok/s on the workload's own steps (one batch of w.T pool tokens
+    per oracle forward), all host threads and one thread."""
+    import oracle
+    xs = np.concatenate(pool_np)
+    lg = oracle.router_logits(xs, wr, bias)
+    ids, _, _ = oracle.select_topk(lg, w.k)
+    g, u, d = datagen.expert_weights(w, experts=np.unique(ids))
+    L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
+    out = {}
+    cores = oracle.max_threads()
+    for threads, budget in ((cores, budget_s), (1, budget_s)):
+        oracle.set_threads(threads)
+        L.forward(pool_np[0])                     # warm
+        n, dt = _timed(lambda i: L.forward(pool_np[i % POOL]), budget, POOL)
+        out[threads] = {"value": n * w.T / dt, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                        "sample": f"{n} steps of the workload ({w.T} pool token(s) per oracle call), {dt:.1f} s"}
+    oracle.set_threads(cores)
+    line = dict(out[cores])
+    line["single_thread"] = out[1]
+    return line
+
+
+def oracle_prefill_rates(w, wr, bias, x, sample_all=256, sample_one=8):
+    """Prefill: routing of all T tokens plus the expert FFNs of a seeded token
+    sample, extrapolated per token to T (all threads: 256 tokens; one thread:
+    8 tokens)."""
+    import oracle
+    cores = oracle.max_threads()
+    lg = oracle.router_logits(x, wr, bias)
+    ids, _, _ = oracle.select_topk(lg, w.k)
+    rng = np.random.default_rng(1)
+    sample = np.sort(rng.choice(w.T, sample_all, replace=False))
+    need = np.unique(ids[sample])
+    g, u, d = datagen.expert_weights(w, experts=need)
+    L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
+    out = {}
+    for threads, n_s in ((cores, sample_all), (1, sample_one)):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        lg = oracle.router_logits(x, wr, bias)
+        oracle.select_topk(lg, w.k)
+        t_route = time.perf_counter() - t0
+        t0 = time.perf_counter()
+        L.forward(x, tokens=sample[:n_s])
+        t_ffn = time.perf_counter() - t0
+        t_tot = t_route + t_ffn * w.T / n_s
+        out[threads] = {"value": w.T / t_tot, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                        "sample": (f"routing of all {w.T} tokens ({t_route:.1f} s) + expert FFNs of {n_s} seeded "
+                                   f"tokens ({t_ffn:.1f} s), extrapolated per token to {w.T}")}
+    oracle.set_threads(cores)
+    line = dict(out[cores])
+    line["single_thread"] = out[1]
+    return line
+
+
+def oracle_stack_rates(w, x_batch, n_one=1):
+    """Stacked NVFP4 layers: the oracle's own quantisation of each layer's
+    bf16 weights (the experts its own routing picks; untimed), then the timed
+    forward of the step: per layer RMSNorm, layer, residual add."""
+    import oracle
+    cores = oracle.max_threads()
+    packs, routers = [], []
+    cur = x_batch
+    for li in range(w.layers):        # untimed preparation, following the oracle's own routing
+        wr = datagen.router_weights(w, li)
+        u_in = oracle.rmsnorm(cur, 1e-6)
+        ids, _, _ = oracle.select_topk(oracle.router_logits(u_in, wr), w.k)
+        need = np.unique(ids)
+        g, u, d = datagen.expert_weights(w, li, experts=need)
+        host = {}
+        for name, arr in (("gate", g), ("up", u), ("down", d)):
+            E, rows, K = arr.shape
+            q = np.zeros((E, rows, K // 2), np.uint8)
+            s = np.zeros((E, rows, K // 16), np.uint8)
+            gs = np.ones(E, np.float32)
+            for e in need:
+                q[e], s[e], gs[e] = oracle.quantize_nvfp4(arr[e])
+            host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
+        L = oracle.Layer(wr, k=w.k, nvfp4=host)
+        cur = oracle.residual_add(cur, L.forward(u_in)["y"])
+        packs.append(L)
+        routers.append(wr)
+
+    def step(xb):
+        c = xb
+        for L in packs:
+            u_in = oracle.rmsnorm(c, 1e-6)
+            c = oracle.residual_add(c, L.forward(u_in)["y"])
+        return c
+
+    out = {}
+    for threads, n_tok in ((cores, w.T), (1, n_one)):
+        oracle.set_threads(threads)
+        t0 = time.perf_counter()
+        step(x_batch[:n_tok])
+        dt = time.perf_counter() - t0
+        out[threads] = {"value": n_tok / dt, "unit": "tok/s", "cores": threads, "kind": "oracle",
+                        "sample": (f"one step: {n_tok} token(s) through all {w.layers} layers ({dt:.1f} s); the "
+                                   "oracle quantises the experts its own routing picks, untimed")}
+    oracle.set_threads(cores)
+    line = dict(out[cores])
+    line["single_thread"] = out[1]
+    return line
 
 
 def run_reference(args):
-    """The reference arm: the CPU oracle timed on the host cores."""
+    """The reference arm: the CPU oracle timed on the host cores, on the
+    headline workload's steps (one pool batch per oracle forward)."""
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
     import oracle
-    w = datagen.WORKLOADS[args.workload]
-    if w.fmt != "bf16" or w.layers != 1:
-        print(json.dumps({"impl": "reference", "unavailable": "reference arm runs the bf16 single-layer workloads"}))
+    name = HEADLINE if args.workload == "all" else args.workload
+    w = datagen.WORKLOADS[name]
+    if w.fmt != "bf16" or w.layers != 1 or w.T > 16:
+        print(json.dumps({"impl": "reference", "unavailable": "reference arm runs the bf16 decode workloads"}))
         return 0
-    pool = [datagen.tokens(w, w.T, start_row=i * w.T) for i in range(POOL)]
+    pool = token_pool(w, 0)
     wr = datagen.router_weights(w)
     bias = datagen.router_bias(w)
     lg = oracle.router_logits(np.concatenate(pool), wr, bias)
     ids, _, _ = oracle.select_topk(lg, w.k)
     g, u, d = datagen.expert_weights(w, experts=np.unique(ids))
     L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
-    # one step = the oracle forward of one batch; bound the whole run to ~150 s
-    t0 = time.perf_counter()
-    L.forward(pool[0])
-    t_step = time.perf_counter() - t0
-    tokens_per_step = w.T
-    sample = "full batch per step"
-    if t_step * (args.steps + args.warmup) > 150.0 and w.T > 1:
-        tokens_per_step = max(1, int(w.T * 150.0 / (t_step * (args.steps + args.warmup))))
-        sample = f"first {tokens_per_step} of {w.T} tokens per step"
     for s in range(args.warmup):
-        L.forward(pool[s % POOL][:tokens_per_step])
+        L.forward(pool[s % POOL])
     t0 = time.perf_counter()
     for s in range(args.steps):
-        L.forward(pool[s % POOL][:tokens_per_step])
+        L.forward(pool[s % POOL])
     total = time.perf_counter() - t0
-    value = tokens_per_step * args.steps / total
+    value = w.T * args.steps / total
+    sample = f"{args.steps} steps of the workload ({w.T} pool token(s) per oracle call)"
     line = {"metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
@@ -255,19 +372,225 @@ def run_reference(args):
 # the CUDA arm
 # ---------------------------------------------------------------------------
 
-def build_gpu_layer(moe, w: datagen.Workload, device, layer: int = 0):
+class Ctx:
+    """Per-process state of the CUDA arm."""
+
+    def __init__(self, args, moe, device, dist, rank, world, local_rank):
+        import torch
+        self.args, self.moe, self.device, self.dist = args, moe, device, dist
+        self.rank, self.world, self.local_rank = rank, world, local_rank
+        self.flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.peaks, self.peak_src = load_peaks()
+
+    def bf(self, a):
+        import torch
+        return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(self.device)
+
+
+def timed_steps(ctx, run_step, steps, warmup, per_step_launches, before_timed=None):
+    """Warm-up, then `steps` steps each preceded by an L2 flush (outside the
+    step's events). before_timed() runs between the two (e.g. to start the
+    library's per-kernel event recording). Returns (per-step ms array,
+    clocks, launches)."""
     import torch
-    wr = datagen.router_weights(w, layer)
-    bias = datagen.router_bias(w, layer)
-    g, u, d = datagen.expert_weights(w, layer)
+    stream = torch.cuda.current_stream()
+    for s in range(warmup):
+        ctx.flush.zero_()
+        run_step(s)
+    torch.cuda.synchronize()
+    if before_timed is not None:
+        before_timed()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    if ctx.dist is not None:
+        ctx.dist.barrier()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(ctx.local_rank)
+    clocks.start()
+    launches = 0
+    for s in range(steps):
+        ctx.flush.zero_()
+        evs[s][0].record(stream)
+        run_step(s)
+        evs[s][1].record(stream)
+        launches += per_step_launches()
+    torch.cuda.synchronize()
+    if ctx.dist is not None:
+        ctx.dist.barrier()
+    clk = clocks.stop()
+    return np.array([a.elapsed_time(b) for a, b in evs], np.float64), clk, launches
 
-    def bf(a):
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
 
-    gl = moe.MoeLayer(bf(wr), w_gate=bf(g), w_up=bf(u), w_down=bf(d),
-                      router_bias=None if bias is None else torch.from_numpy(bias).to(device),
-                      top_k=w.k, max_tokens=max(w.T, 16))
-    return gl, (wr, bias, g, u, d)
+def e2e_host(ctx, w, pool_np, call, n_steps):
+    """End to end through the C ABI from pinned host memory: every step copies
+    its tokens in, runs the layer(s), copies the result out and waits."""
+    import torch
+    xh = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16).pin_memory() for p in pool_np]
+    oh = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    for s in range(3):
+        call(xh[s % POOL], oh)
+    t0 = time.perf_counter()
+    for s in range(n_steps):
+        call(xh[s % POOL], oh)
+    dt = time.perf_counter() - t0
+    v, _ = aggregate(w.T * n_steps, dt, ctx.dist, ctx.device)
+    return {"value": v, "unit": "tok/s", "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,
+            "steps": n_steps, "note": "pinned host tokens -> device, the step, result -> pinned host, stream sync; "
+                                      "no L2 flush"}
+
+
+def unique_experts(gl, pool):
+    return np.array([int((gl.route(p)["counts"] > 0).sum().item()) for p in pool], np.float64)
+
+
+def measure_decode(ctx, w, gl, host):
+    """bf16 decode (T <= 16): one persistent launch per step."""
+    import torch
+    args = ctx.args
+    pool_np = token_pool(w, ctx.rank)
+    pool = [ctx.bf(p) for p in pool_np]
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=ctx.device)
+    step_ms, clk, launches = timed_steps(ctx, lambda s: gl.forward(pool[s % POOL], out), args.steps, args.warmup,
+                                         gl.last_launch_count, lambda: gl.profile_begin(args.steps))
+    prof = gl.profile_end()
+    assert gl.device_status() == 0, "device error"
+    total_s = float(step_ms.sum()) / 1e3
+    value, t_max = aggregate(w.T * args.steps, total_s, ctx.dist, ctx.device)
+    U = unique_experts(gl, pool)[np.arange(args.steps) % POOL]
+    layer_bytes = U * w.expert_bytes_bf16 + w.E * w.d * 2          # active experts + router
+    hbm = ctx.peaks["hbm_gbs"]
+    k_ms = prof[:, 0].astype(np.float64)
+    ach = float(layer_bytes.mean() / (k_ms.mean() / 1e3) / 1e9)
+    roof = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+            "frac": ach / hbm, "traffic": measured_traffic(w.name) if not args.experts else None,
+            "peak_source": ctx.peak_src, "bytes_per_launch": float(layer_bytes.mean()),
+            "bytes_rule": "unique active experts x 3*d*I*2 B + router E*d*2 B",
+            "unique_experts_per_step": float(U.mean()), "ms_per_launch": float(k_ms.mean())}
+    res = {"value": value, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": t_max * 1e3 / args.steps, "roofline": roof, "gpu_launches": launches, "clocks": clk,
+           "config": workload_config(w, l2="flushed before every step (256 MiB write), outside the step events")}
+    res["e2e"] = e2e_host(ctx, w, pool_np, gl.forward_host, min(args.e2e_steps, args.steps))
+    if ctx.rank == 0 and not args.no_cpu_baseline:
+        wr, bias = host
+        res["cpu_baseline"] = oracle_decode_rates(w, wr, bias, pool_np)
+    return res
+
+
+def measure_prefill(ctx, w, gl, host):
+    """bf16 prefill (T = 4096): routing, gather, two grouped tcgen05 GEMMs, combine."""
+    import torch
+    args = ctx.args
+    n_pool = 4                                   # 4 distinct 4096-token batches
+    pool_np = [datagen.tokens(w, w.T, start_row=(ctx.rank * n_pool + i) * w.T) for i in range(n_pool)]
+    pool = [ctx.bf(p) for p in pool_np]
+    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=ctx.device)
+    step_ms, clk, launches = timed_steps(ctx, lambda s: gl.forward(pool[s % n_pool], out), args.steps, args.warmup,
+                                         gl.last_launch_count, lambda: gl.profile_begin(args.steps))
+    prof = gl.profile_end()                      # [steps, 3] = route + gather, expert GEMMs, combine
+    assert gl.device_status() == 0, "device error"
+    total_s = float(step_ms.sum()) / 1e3
+    value, t_max = aggregate(w.T * args.steps, total_s, ctx.dist, ctx.device)
+    U = np.array([int((gl.route(p)["counts"] > 0).sum().item()) for p in pool], np.float64)
+    flops = 2.0 * w.T * w.k * 3 * w.d * w.I
+    ex_ms = prof[:, 1].astype(np.float64)
+    tf = flops / (ex_ms.mean() / 1e3) / 1e12
+    peak_tf = ctx.peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
+    wbytes = float(U.mean()) * w.expert_bytes_bf16
+    gbs = wbytes / (ex_ms.mean() / 1e3) / 1e9
+    hbm = ctx.peaks["hbm_gbs"]
+    # at T = 4096 the expert GEMMs' weight stream outlasts their arithmetic
+    # (128 FLOP/B < the ridge point), so HBM is the binding ceiling
+    roof = {"kernel": "grouped_gemm_kernel (gate/up + down)", "bound": "hbm", "achieved": gbs, "peak": hbm,
+            "unit": "GB/s", "frac": gbs / hbm, "traffic": None, "peak_source": ctx.peak_src,
+            "bytes_per_launch": wbytes, "bytes_rule": "unique active experts x 3*d*I*2 B (weights read once)",
+            "ms_per_launch": float(ex_ms.mean()),
+            "tensor": {"achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf,
+                       "flops_per_launch": flops,
+                       "ceiling_frac": (flops / peak_tf / 1e12) / max(flops / peak_tf / 1e12, wbytes / hbm / 1e9)}}
+    kernel_ms = {"route_gather": float(prof[:, 0].mean()), "expert_gemms": float(ex_ms.mean()),
+                 "combine": float(prof[:, 2].mean())}
+    res = {"value": value, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": t_max * 1e3 / args.steps, "roofline": roof, "kernel_ms": kernel_ms,
+           "gpu_launches": launches, "clocks": clk,
+           "config": workload_config(w, tokens=f"pool of {n_pool} seeded 4096-token batches",
+                                     l2="flushed before every step (256 MiB write), outside the step events")}
+    res["e2e"] = e2e_host(ctx, w, pool_np, gl.forward_host, min(args.e2e_steps, args.steps, 20))
+    if ctx.rank == 0 and not args.no_cpu_baseline:
+        wr, bias = host
+        res["cpu_baseline"] = oracle_prefill_rates(w, wr, bias, pool_np[0])
+    return res
+
+
+def build_stack(ctx, w):
+    """The stacked workload's NVFP4 layers, quantised on the GPU from the
+    seeded bf16 weights (quantisation is set-up, not part of a step)."""
+    import torch
+    moe = ctx.moe
+    layers = []
+    for li in range(w.layers):
+        wr = datagen.router_weights(w, li)
+        g, u, d = datagen.expert_weights(w, li)
+        packs = {}
+        for name, arr in (("gate", g), ("up", u), ("down", d)):
+            dev = ctx.bf(arr)
+            packs["q_" + name], packs["s_" + name], packs["g_" + name] = moe.quantize_nvfp4(dev)
+            del dev
+        del g, u, d
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        layers.append(moe.MoeLayer(ctx.bf(wr), nvfp4=packs, top_k=w.k, max_tokens=max(w.T, 16)))
+    return layers
+
+
+def measure_stack(ctx, w, layers):
+    """8 NVFP4 layers, each RMSNorm -> MoE -> residual, in one launch per step."""
+    import torch
+    args, moe = ctx.args, ctx.moe
+    pool_np = token_pool(w, ctx.rank)
+    pool = [ctx.bf(p) for p in pool_np]
+    stack = moe.MoeStack(layers)
+    xcur = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=ctx.device)
+
+    def step(s):
+        xcur.copy_(pool[s % POOL])
+        stack.forward(xcur, out=xcur, eps=1e-6)
+
+    step_ms, clk, launches = timed_steps(ctx, step, args.steps, args.warmup, lambda: 1)
+    assert layers[0].device_status() == 0, "device error"
+    total_s = float(step_ms.sum()) / 1e3
+    value, t_max = aggregate(w.T * args.steps, total_s, ctx.dist, ctx.device)
+    # unique experts per layer per pool batch, from an untimed layer-by-layer replay
+    U = np.zeros((POOL, w.layers))
+    ubuf = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=ctx.device)
+    for i in range(POOL):
+        xcur.copy_(pool[i])
+        for li, gl in enumerate(layers):
+            moe.rmsnorm(xcur, 1e-6, out=ubuf)
+            U[i, li] = int((gl.route(ubuf)["counts"] > 0).sum().item())
+            gl.forward(ubuf, out=xcur, res=xcur)
+    torch.cuda.synchronize()
+    Us = U[np.arange(args.steps) % POOL]                               # [steps, layers]
+    layer_bytes = Us * w.expert_bytes_nvfp4 + w.E * w.d * 2           # [steps, layers]
+    step_bytes = layer_bytes.sum(1)
+    hbm = ctx.peaks["hbm_gbs"]
+    # the stacked launch is the step (plus one 32 KB token copy)
+    ach = float(step_bytes.mean() / (step_ms.mean() / 1e3) / 1e9)
+    roof = {"kernel": f"decode_layer_kernel (NVFP4, {w.layers} layers in one launch)", "bound": "hbm",
+            "achieved": ach, "peak": hbm, "unit": "GB/s", "frac": ach / hbm, "traffic": None,
+            "peak_source": ctx.peak_src, "bytes_per_launch": float(step_bytes.mean()),
+            "bytes_rule": "sum over layers of unique active experts x 10,616,832 B (NVFP4 codes + block scales) "
+                          "+ router E*d*2 B",
+            "unique_experts_per_layer": float(Us.mean()), "ms_per_launch": float(step_ms.mean())}
+    res = {"value": value, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
+           "ms_per_step": t_max * 1e3 / args.steps, "roofline": roof, "gpu_launches": launches, "clocks": clk,
+           "dtype": "nvfp4 experts, bf16 activations, fp32 accumulate",
+           "config": workload_config(w, step=f"{w.layers} x (RMSNorm, MoE, residual), one launch",
+                                     l2="flushed before every step (256 MiB write), outside the step events")}
+    res["e2e"] = e2e_host(ctx, w, pool_np, lambda xh, oh: stack.forward_host(xh, oh, eps=1e-6),
+                          min(args.e2e_steps, args.steps))
+    if ctx.rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = oracle_stack_rates(w, pool_np[0])
+    stack.close()
+    return res
 
 
 def run_ours(args):
@@ -280,272 +603,61 @@ def run_ours(args):
     dist = init_dist(world, "nccl")
     import top_moe_expert_router_gb300 as moe
     moe.load()
-    w = datagen.WORKLOADS[args.workload]
-    if args.experts:
-        import dataclasses
-        w = dataclasses.replace(w, E=args.experts)
-    if w.layers != 1 or w.fmt != "bf16":
-        return run_stack(args, w, moe, device, dist, rank, world, local_rank)
-    gl, host = build_gpu_layer(moe, w, device)
-    # each rank draws its own token pool (distinct rows of the token stream)
-    pool_np = [datagen.tokens(w, w.T, start_row=(rank * POOL + i) * w.T) for i in range(POOL)]
-    pool = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16).to(device) for p in pool_np]
-    out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream()
+    ctx = Ctx(args, moe, device, dist, rank, world, local_rank)
+    names = ORDER if args.workload == "all" else [args.workload]
+    results = {}
 
-    for s in range(args.warmup):
-        flush.zero_()
-        gl.forward(pool[s % POOL], out)
-    torch.cuda.synchronize()
-    assert gl.device_status() == 0, "device error during warm-up"
-
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    gl.profile_begin(args.steps)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    launches = 0
-    for s in range(args.steps):
-        flush.zero_()
-        evs[s][0].record(stream)
-        gl.forward(pool[s % POOL], out)
-        evs[s][1].record(stream)
-        launches += gl.last_launch_count()
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-    step_ms = np.array([a.elapsed_time(b) for a, b in evs])
-    # decode: [steps, 4] = route, gate/up, down, combine
-    # prefill: [steps, 3] = route + gather, grouped GEMMs, combine
-    prof = gl.profile_end()
-    status = gl.device_status()
-    assert status == 0, f"device error {status}"
-    total_s = float(step_ms.sum()) / 1e3
-    value, t_max = aggregate(w.T * args.steps, total_s, dist, device)
-
-    # unique experts per step (for the bytes each step must stream)
-    uniq = []
-    for p in pool:
-        r = gl.route(p)
-        uniq.append(int((r["counts"] > 0).sum().item()))
-    U = np.array([uniq[s % POOL] for s in range(args.steps)], np.float64)
-    eb = w.expert_bytes_bf16
-    gateup_bytes = U * 2 * w.I * w.d * 2                # W_gate + W_up rows of the active experts
-    layer_bytes = U * eb + w.E * w.d * 2                # all active expert weights + router
-    peaks, peak_src = load_peaks()
-    hbm = peaks["hbm_gbs"]
-    step_gbs = float(layer_bytes.sum() / total_s / 1e9)
-    if prof.shape[1] == 1:
-        # the whole layer is one persistent kernel: router, routing, expert stream, combine
-        ly_ms = prof[:, 0].astype(np.float64)
-        ly_gbs = float(layer_bytes.mean() / (ly_ms.mean() / 1e3) / 1e9)
-        roofline = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": ly_gbs, "peak": hbm,
-                    "unit": "GB/s", "frac": ly_gbs / hbm,
-                    "traffic": measured_traffic(args.workload) if not args.experts else None,
-                    "peak_source": peak_src,
-                    "bytes_per_launch": float(layer_bytes.mean()), "ms_per_launch": float(ly_ms.mean())}
-        kernel_ms = {"layer": float(ly_ms.mean())}
-    elif prof.shape[1] == 4:
-        gu_ms = prof[:, 1].astype(np.float64)
-        gu_gbs = float(gateup_bytes.mean() / (gu_ms.mean() / 1e3) / 1e9)
-        roofline = {"kernel": "decode_gateup_kernel", "bound": "hbm", "achieved": gu_gbs, "peak": hbm,
-                    "unit": "GB/s", "frac": gu_gbs / hbm, "traffic": None, "peak_source": peak_src,
-                    "bytes_per_launch": float(gateup_bytes.mean()), "ms_per_launch": float(gu_ms.mean())}
-        kernel_ms = {"route": float(prof[:, 0].mean()), "gateup": float(gu_ms.mean()),
-                     "down": float(prof[:, 2].mean()), "combine": float(prof[:, 3].mean())}
-    else:
-        # expert GEMMs: 2 FLOP x rows (T*k) x (2*d*I gate/up + d*I down)
-        flops = 2.0 * w.T * w.k * 3 * w.d * w.I
-        ex_ms = prof[:, 1].astype(np.float64)
-        tf = flops / (ex_ms.mean() / 1e3) / 1e12
-        peak_tf = peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops"))
-        roofline = {"kernel": "grouped_gemm_kernel (gate/up + down)", "bound": "tensor", "achieved": tf,
-                    "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf, "traffic": None,
-                    "peak_source": peak_src, "flops_per_launch": flops, "ms_per_launch": float(ex_ms.mean()),
-                    "hbm_frac_of_expert_stage": float(U.mean() * eb / (ex_ms.mean() / 1e3) / 1e9 / hbm)}
-        kernel_ms = {"route_gather": float(prof[:, 0].mean()), "expert_gemms": float(ex_ms.mean()),
-                     "combine": float(prof[:, 2].mean())}
-
-    # end to end through the C ABI from pinned host memory
-    e2e = None
-    if rank == 0 or True:
-        xh = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16).pin_memory() for p in pool_np]
-        oh = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
-        for s in range(5):
-            gl.forward_host(xh[s % POOL], oh)
-        n_e2e = min(args.e2e_steps, args.steps)
-        t0 = time.perf_counter()
-        for s in range(n_e2e):
-            gl.forward_host(xh[s % POOL], oh)
-        e2e_s = time.perf_counter() - t0
-        e2e_v, _ = aggregate(w.T * n_e2e, e2e_s, dist, device)
-        e2e = {"value": e2e_v, "unit": "tok/s", "h2d_bytes_per_step": w.T * w.d * 2,
-               "d2h_bytes_per_step": w.T * w.d * 2, "steps": n_e2e,
-               "note": "moe_forward_host: H2D copy, layer, D2H copy, stream sync per step; no L2 flush"}
-
-    cpu = None
-    if rank == 0 and world >= 1 and not args.no_cpu_baseline:
-        import oracle
-        wr, bias, g, u, d = host
-        L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
-        n_tok = 32
-        xs = np.concatenate(pool_np)[:n_tok]
-        rate, dt, cores = oracle_token_rate(L, xs)
-        cpu = {"value": rate, "unit": "tok/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n_tok} tokens of the pool, full layer each, one oracle call ({dt:.1f} s)"}
-
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(w, parallelism=f"replicas x{world}, tokens split by rank",
-                                      l2="flushed before every step (256 MiB write), outside the step events"),
-            "roofline": roofline,
-            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
-                              "frac": step_gbs / hbm, "bytes_per_step": float(layer_bytes.mean()),
-                              "unique_experts_per_step": float(U.mean()), "kernel_ms": kernel_ms},
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": launches,
-            "clocks": clk,
-        }
-        print(json.dumps(line))
-    if dist is not None:
-        dist.barrier()
-        dist.destroy_process_group()
-    return 0
-
-
-def run_stack(args, w, moe, device, dist, rank, world, local_rank):
-    """Stacked NVFP4 decode: every step runs the token batch through all
-    layers, each RMSNorm -> MoE (NVFP4 experts) -> residual add."""
-    import torch
-
-    def bf(a):
-        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
-
-    layers, host_routers = [], []
-    for li in range(w.layers):
-        wr = datagen.router_weights(w, li)
-        g, u, d = datagen.expert_weights(w, li)
-        packs = {}
-        for name, arr in (("gate", g), ("up", u), ("down", d)):
-            dev = bf(arr)
-            q, s, gs = moe.quantize_nvfp4(dev)
-            packs["q_" + name], packs["s_" + name], packs["g_" + name] = q, s, gs
-            del dev
-        torch.cuda.synchronize()
+    bf16_names = [n for n in names if datagen.WORKLOADS[n].fmt == "bf16"]
+    if bf16_names:
+        # decode and prefill share the layer's weights (seed 0, layer 0);
+        # prefill adds the skewed router bias
+        w0 = datagen.WORKLOADS[bf16_names[0]]
+        if args.experts:
+            w0 = dataclasses.replace(w0, E=args.experts)
+        wr = datagen.router_weights(w0)
+        g, u, d = datagen.expert_weights(w0)
+        dev = {"wr": ctx.bf(wr), "gate": ctx.bf(g), "up": ctx.bf(u), "down": ctx.bf(d)}
+        del g, u, d
+        for n in bf16_names:
+            w = datagen.WORKLOADS[n]
+            if args.experts:
+                w = dataclasses.replace(w, E=args.experts)
+            bias = datagen.router_bias(w)
+            gl = moe.MoeLayer(dev["wr"], w_gate=dev["gate"], w_up=dev["up"], w_down=dev["down"],
+                              router_bias=None if bias is None else torch.from_numpy(bias).to(device),
+                              top_k=w.k, max_tokens=max(w.T, 16))
+            fn = measure_prefill if w.T > 16 else measure_decode
+            results[n] = fn(ctx, w, gl, (wr, bias))
+            gl.close()
+            torch.cuda.empty_cache()
+        del dev
         torch.cuda.empty_cache()
-        layers.append(moe.MoeLayer(bf(wr), nvfp4=packs, top_k=w.k, max_tokens=max(w.T, 16)))
-        host_routers.append(wr)
-    pool_np = [datagen.tokens(w, w.T, start_row=(rank * POOL + i) * w.T) for i in range(POOL)]
-    pool = [bf(p) for p in pool_np]
-    xcur = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=device)
-    ubuf = torch.empty_like(xcur)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
-    stream = torch.cuda.current_stream()
+    for n in names:
+        w = datagen.WORKLOADS[n]
+        if w.fmt == "nvfp4":
+            if args.experts:
+                w = dataclasses.replace(w, E=args.experts)
+            layers = build_stack(ctx, w)
+            results[n] = measure_stack(ctx, w, layers)
+            for gl in layers:
+                gl.close()
+            del layers
+            torch.cuda.empty_cache()
 
-    # the whole stack in one launch when the batch fits (T <= 8)
-    stack = moe.MoeStack(layers) if w.T <= 8 else None
-
-    def step(x0, route_log=None):
-        xcur.copy_(x0)
-        if stack is not None and route_log is None:
-            stack.forward(xcur, out=xcur, eps=1e-6)
-            return
-        for gl in layers:
-            moe.rmsnorm(xcur, 1e-6, out=ubuf)
-            if route_log is not None:
-                route_log.append(int((gl.route(ubuf)["counts"] > 0).sum().item()))
-            gl.forward(ubuf, out=xcur, res=xcur)
-
-    for s in range(args.warmup):
-        flush.zero_()
-        step(pool[s % POOL])
-    torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for gl in layers:
-        gl.profile_begin(args.steps)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(local_rank)
-    clocks.start()
-    launches = 0
-    for s in range(args.steps):
-        flush.zero_()
-        evs[s][0].record(stream)
-        step(pool[s % POOL])
-        evs[s][1].record(stream)
-        launches += 1 if stack is not None else w.layers * (1 + layers[0].last_launch_count())
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-    step_ms = np.array([a.elapsed_time(b) for a, b in evs])
-    profs = [gl.profile_end() for gl in layers]             # each [steps, 4] (empty for the stacked launch)
-    for gl in layers:
-        assert gl.device_status() == 0
-    total_s = float(step_ms.sum()) / 1e3
-    value, t_max = aggregate(w.T * args.steps, total_s, dist, device)
-    # unique experts per layer per step, from an untimed replay of the pool
-    U = np.zeros((POOL, w.layers))
-    for i in range(POOL):
-        log = []
-        step(pool[i], route_log=log)
-        U[i] = log
-    torch.cuda.synchronize()
-    Us = np.array([U[s % POOL] for s in range(args.steps)])      # [steps, layers]
-    eb = w.expert_bytes_nvfp4
-    peaks, peak_src = load_peaks()
-    hbm = peaks["hbm_gbs"]
-    layer_bytes = Us * eb + w.E * w.d * 2                           # [steps, layers]
-    if stack is not None:
-        # one stacked launch per step: its bytes are all layers' bytes, its
-        # time the step's (the step adds one 32 KB token copy)
-        kname = f"decode_layer_kernel (NVFP4, {w.layers} layers in one launch)"
-        k_bytes = layer_bytes.sum(1, keepdims=True)
-        k_ms = step_ms[:, None].astype(np.float64)
-        kms = {"stack": float(k_ms.mean()), "per_layer": float(k_ms.mean() / w.layers)}
-    elif profs[0].shape[1] == 1:
-        kname = "decode_layer_kernel (NVFP4)"
-        k_bytes = layer_bytes
-        k_ms = np.stack([p[:, 0] for p in profs], axis=1).astype(np.float64)
-        kms = {"layer": float(k_ms.mean())}
-    else:
-        kname = "decode_gateup_kernel (NVFP4)"
-        k_bytes = Us * 2 * w.I * (w.d // 2 + w.d // 16)             # gate + up codes and scales
-        k_ms = np.stack([p[:, 1] for p in profs], axis=1).astype(np.float64)
-        kms = {name: float(np.mean([p[:, i].mean() for p in profs]))
-               for i, name in enumerate(["route", "gateup", "down", "combine"])}
-    gu_bytes, gu_ms = k_bytes, k_ms
-    gu_gbs = float(gu_bytes.sum() / (gu_ms.sum() / 1e3) / 1e9)
-    step_bytes = layer_bytes.sum(1)
-    step_gbs = float(step_bytes.sum() / total_s / 1e9)
     if rank == 0:
+        head_name = HEADLINE if HEADLINE in results else names[0]
+        head = results[head_name]
         line = {
-            "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": t_max * 1e3 / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "nvfp4 experts, bf16 activations, fp32 accumulate",
-            "data": "synthetic",
-            "config": workload_config(w, parallelism=f"replicas x{world}",
-                                      l2="flushed before every step (256 MiB write), outside the step events",
-                                      step="8 x (RMSNorm, MoE, residual)" + (", one launch" if stack is not None else "")),
-            "roofline": {"kernel": kname, "bound": "hbm", "achieved": gu_gbs, "peak": hbm,
-                         "unit": "GB/s", "frac": gu_gbs / hbm, "traffic": None, "peak_source": peak_src,
-                         "bytes_per_launch": float(gu_bytes.mean()), "ms_per_launch": float(gu_ms.mean())},
-            "step_roofline": {"bound": "hbm", "achieved": step_gbs, "peak": hbm, "unit": "GB/s",
-                              "frac": step_gbs / hbm, "bytes_per_step": float(step_bytes.mean()),
-                              "unique_experts_per_layer": float(Us.mean()), "kernel_ms_per_layer": kms},
-            "cpu_baseline": None,
-            "e2e": None,
-            "gpu_launches": launches,
-            "clocks": clk,
+            "metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": head.get("dtype", "bf16"), "data": "synthetic",
+            "config": dict(head["config"], parallelism=f"replicas x{world}, tokens split by rank"),
+            "roofline": head["roofline"],
+            "cpu_baseline": head.get("cpu_baseline"),
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "workloads": {n: results[n] for n in names},
         }
         print(json.dumps(line))
     if dist is not None:

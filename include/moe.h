@@ -133,6 +133,28 @@ moe_status moe_forward_host(moe_layer *layer, const void *x_host, void *out_host
  * output precision) and are widened to fp32 here. */
 moe_status moe_debug_expert_outputs(moe_layer *layer, float *Y, int T, void *stream);
 
+/* Routing records of the last forward or route on this layer, as the
+ * kernels left them in the workspace (no recomputation): the fields of
+ * moe_route, same layouts; any output pointer may be NULL. A forward of
+ * T <= 16 tokens leaves the records its single decode launch computed and
+ * published; a larger forward leaves those of the large-batch routing
+ * kernels, or, where it runs in chunks of 16 tokens, those of its last
+ * chunk. T must be the last call's token count. For parity checks of the
+ * routing each forward path uses. */
+moe_status moe_debug_route_records(moe_layer *layer, int T, int32_t *ids, float *w, int32_t *counts,
+                                   int32_t *offsets, int32_t *perm, int32_t *pos, void *stream);
+
+/* Test hook for the device-side failure detection. While hold != 0, every
+ * grid barrier of this layer's single-launch decode kernel (T <= 16, and
+ * moe_stack_forward on a stack whose first layer is this one) waits for one
+ * arrival more than the grid provides, so its bounded wait (1.5 s) runs out:
+ * the launch unwinds without computing the experts, leaves `out` undefined
+ * and sets the timeout bit that moe_get_device_status() reports as
+ * MOE_ERR_TIMEOUT. hold = 0 restores normal operation; the next call runs
+ * normally (the launch that gave up resets its counters on exit). Enqueued on
+ * `stream` (one 4-byte host-to-device copy). */
+moe_status moe_debug_hold_grid_barrier(moe_layer *layer, int hold, void *stream);
+
 /* Row-wise RMSNorm without a learned scale: out = x / sqrt(mean(x^2) + eps),
  * x and out [T, d] bf16 (out may alias x), fp32 arithmetic. */
 moe_status moe_rmsnorm(const void *x, void *out, int T, int d, float eps, void *stream);
@@ -172,17 +194,24 @@ moe_status moe_profile_end(moe_layer *layer, float *ms_host, int max_kernels, in
  * MOE_STATIC_SCRATCH_BYTES that every GPU which loads libmoe.so holds until
  * the process exits. The call allocates nothing (no cudaMalloc, no
  * allocating library routine). desc is read on the host during the call only;
- * its max_tokens is not used. x [T, d] and out [T, d] are bf16 device
- * buffers of the caller.
- * - The first call on a device, with that device current, looks up the
- *   array's device address (cudaGetSymbolAddress); make that first call
+ * its max_tokens is ignored (the shape is checked as if it were T). x [T, d]
+ * and out [T, d] are bf16 device buffers of the caller.
+ * - Every call, with the caller's device and context current, looks up the
+ *   array's device address in that context (cudaGetSymbolAddress; nothing is
+ *   cached, so a new context after cudaDeviceReset, or a context of the
+ *   caller's own on the same device, gets its own copy of the array). The
+ *   first call in a process may load the library's device code: make it
  *   before any stream capture.
  * - Every call shares the one array and clears its control words at the start
  *   (an async memset on `stream`): calls that overlap on the GPU race, so
  *   issue them on one stream or otherwise order them.
- * - Shapes whose scratch exceeds MOE_STATIC_SCRATCH_BYTES, or T > 16, return
- *   MOE_ERR_UNSUPPORTED / MOE_ERR_INVALID_ARG before any GPU work.
- * - Device-side error bits are not reported (use moe_forward for that). */
+ * - Shapes whose scratch exceeds MOE_STATIC_SCRATCH_BYTES, or whose tokens do
+ *   not fit in shared memory beside the weight ring, return
+ *   MOE_ERR_UNSUPPORTED; T outside [1, 16] returns MOE_ERR_INVALID_ARG; both
+ *   before any GPU work.
+ * - Device-side error bits (a bounded wait that ran out) are not reported:
+ *   the next call clears them. After such an event `out` is undefined; a
+ *   caller that needs the check uses moe_forward and moe_get_device_status. */
 #define MOE_STATIC_SCRATCH_BYTES (8u << 20)
 moe_status moe_forward_static_scratch(const moe_layer_desc *desc, const void *x, void *out, int T,
                                       void *stream);
@@ -208,6 +237,12 @@ typedef struct moe_stack moe_stack;
 moe_status moe_stack_create(moe_layer *const *layers, int n_layers, moe_stack **out);
 moe_status moe_stack_forward(moe_stack *stack, const void *x, void *out, int T, float eps, void *layer_out,
                              void *stream);
+/* End-to-end stack forward from host memory: copies x_host [T, d] bf16 into
+ * layers[0]'s workspace, runs moe_stack_forward, copies the result to
+ * out_host [T, d] bf16 and waits for the stream. Page-locked host buffers
+ * give asynchronous copies. */
+moe_status moe_stack_forward_host(moe_stack *stack, const void *x_host, void *out_host, int T, float eps,
+                                  void *stream);
 moe_status moe_stack_destroy(moe_stack *stack);
 
 moe_status moe_layer_destroy(moe_layer *layer);

@@ -92,3 +92,33 @@ def test_stack_calls_reject_bad_arguments(lib):
 def test_missing_library_fails_loudly(tmp_path):
     with pytest.raises(OSError):
         ctypes.CDLL(str(tmp_path / "libmoe.so"))
+
+
+def test_debug_and_host_stack_calls_reject_null_handles(lib):
+    assert lib.moe_debug_route_records(None, 1, None, None, None, None, None, None, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_debug_hold_grid_barrier(None, 1, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_stack_forward_host(None, ctypes.c_void_p(4096), ctypes.c_void_p(8192), 1, 1e-6,
+                                      None) == moe.MOE_ERR_INVALID_ARG
+
+
+def _fake_weights(d):
+    """Aligned, non-null pointer values: every case below is rejected on the
+    host before the pointers could be used."""
+    for name in ("w_router", "w_gate", "w_up", "w_down"):
+        setattr(d, name, 1 << 20)
+    return d
+
+
+@pytest.mark.parametrize("kw,T,want", [
+    (dict(), 17, moe.MOE_ERR_INVALID_ARG),                        # more tokens than the decode path takes
+    (dict(), 0, moe.MOE_ERR_INVALID_ARG),
+    (dict(d=8192, I=4096), 16, moe.MOE_ERR_UNSUPPORTED),          # scratch above MOE_STATIC_SCRATCH_BYTES
+    (dict(d=8192, I=1536), 8, moe.MOE_ERR_UNSUPPORTED),           # tokens do not fit in shared memory
+    (dict(top_k=9), 4, moe.MOE_ERR_UNSUPPORTED),
+])
+def test_static_scratch_rejects_before_gpu_work(lib, kw, T, want):
+    d = _fake_weights(_desc(**kw))
+    s = lib.moe_forward_static_scratch(ctypes.byref(d), ctypes.c_void_p(1 << 21), ctypes.c_void_p(1 << 22), T, None)
+    assert s == want
+    assert lib.moe_forward_static_scratch(None, ctypes.c_void_p(1 << 21), ctypes.c_void_p(1 << 22), 1,
+                                          None) == moe.MOE_ERR_INVALID_ARG

@@ -8,7 +8,7 @@ import torch
 
 import datagen
 import oracle
-from moe_testlib import NEAR_TIE, NVFP4_TOL, bf16_host, check_route, normwise_rel_err, to_dev, to_dev_bf16
+from moe_testlib import NVFP4_TOL, bf16_host, check_route, normwise_rel_err, to_dev, to_dev_bf16
 
 pytestmark = pytest.mark.gpu
 
@@ -54,7 +54,7 @@ def _quantize_on_gpu(moe, g, u, d):
     return packs
 
 
-@pytest.mark.parametrize("T", [1, 4, 16])
+@pytest.mark.parametrize("T", [1, 4, 16, 17, 40])
 def test_small_nvfp4_layer(gpu_lib, T):
     w = datagen.Workload("fp4small", T=T, d=512, E=64, k=8, I=256, fmt="nvfp4", router_scale=4.0)
     wr = datagen.router_weights(w)
@@ -67,24 +67,29 @@ def test_small_nvfp4_layer(gpu_lib, T):
         np.testing.assert_array_equal(packs["s_" + name].cpu().numpy(), s)
         np.testing.assert_array_equal(packs["g_" + name].cpu().numpy(), gs)
         host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
-    gl = _nvfp4_gpu_layer(gpu_lib, wr, None, packs, w.k, 16)
+    gl = _nvfp4_gpu_layer(gpu_lib, wr, None, packs, w.k, 64)
     L = oracle.Layer(wr, k=w.k, nvfp4=host)
     x = datagen.tokens(w, T, start_row=3)
     xd = to_dev_bf16(x)
     r = gl.route(xd)
     y = gl.forward(xd)
-    Y = gl.expert_outputs(T)
+    # the forward's own routing records (a single decode launch for T <= 16)
+    rec = gl.route_records(T) if T <= 16 else None
+    Y = gl.expert_outputs(T) if T <= 16 else None
     torch.cuda.synchronize()
     assert gl.device_status() == 0
-    ref = L.forward(x, forced_ids=r["ids"].cpu().numpy(), want_Y=True)
+    ref = L.forward(x, forced_ids=r["ids"].cpu().numpy(), want_Y=T <= 16)
     own = L.forward(x)
     check_route(r, own["ids"], own["w"], own["gap"], w.E)
+    if rec is not None:
+        check_route(rec, own["ids"], own["w"], own["gap"], w.E)
     err = normwise_rel_err(datagen.bf16_to_f32(bf16_host(y)), ref["y"])
     assert err.max() <= NVFP4_TOL
     assert err.max() < 1e-2            # the kernel adds only fp32 rounding to the shared quantisation
-    pos = r["pos"].cpu().numpy()
-    eY = normwise_rel_err(Y.cpu().numpy()[pos], ref["Y"])
-    assert eY.max() < 1e-2
+    if Y is not None:
+        pos = r["pos"].cpu().numpy()
+        eY = normwise_rel_err(Y.cpu().numpy()[pos], ref["Y"])
+        assert eY.max() < 1e-2
 
 
 def test_stacked_nvfp4_decode_full_size(gpu_lib):
@@ -135,4 +140,3 @@ def test_stacked_nvfp4_decode_full_size(gpu_lib):
         del gl, packs
         torch.cuda.empty_cache()
     assert worst < 1e-2
-    assert NEAR_TIE > 0

@@ -250,12 +250,11 @@ def test_expert_relabelling_invariance():
     lab = np.random.default_rng(2).permutation(TINY.E)       # new expert i is old lab[i]
     L2 = oracle.Layer(wr[lab], g[lab], u[lab], d[lab], k=8)
     b = L2.forward(x)
-    inv = np.argsort(lab)
-    for t in range(16):
-        if a["gap"][t] > 1e-3:
-            np.testing.assert_array_equal(lab[b["ids"][t]], a["ids"][t])
-            np.testing.assert_allclose(b["y"][t], a["y"][t], rtol=1e-12, atol=1e-15)
-    assert inv is not None
+    clear = a["gap"] > 1e-3
+    assert clear.sum() >= 8                     # the check below covers most tokens
+    for t in np.flatnonzero(clear):
+        np.testing.assert_array_equal(lab[b["ids"][t]], a["ids"][t])
+        np.testing.assert_allclose(b["y"][t], a["y"][t], rtol=1e-12, atol=1e-15)
 
 
 # --------------------------------------------------------------------------
@@ -430,7 +429,7 @@ def test_expert_norm_is_scale_invariant_and_bounded():
     b1, b2 = (L_.forward(x)["y"] for L_ in big)
     # RMS normalisation removes the scale of W_down
     np.testing.assert_allclose(b2, b1, rtol=1e-6, atol=1e-7)
-    assert np.abs(b1 - 2 * b1).max() > 1e-3
+    assert np.abs(b1).max() > 1e-3               # the invariance is not that of an all-zero output
     # each slot contributes unit RMS: the combined RMS is at most sum(w) = 1
     assert (np.sqrt((a["y"] ** 2).mean(1)) <= 1.0 + 1e-9).all()
     # the raw expert outputs are the same as without the normalisation

@@ -37,11 +37,15 @@ def test_static_scratch_forward_matches_forward(gpu_lib, shape):
     layer = _layer(gpu_lib, w)
     lib = gpu_lib.load()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    # the call ignores max_tokens: the second call passes a copy with 0 there
+    desc0 = gpu_lib.MoeLayerDesc.from_buffer_copy(layer._desc)
+    desc0.max_tokens = 0
     for call, T in enumerate((5, 16)):          # two calls in a row, different token batches
         x = to_dev_bf16(datagen.tokens(w, T, start_row=1000 + 100 * call))
         ref = layer.forward(x)
         out = torch.empty_like(ref)
-        s = lib.moe_forward_static_scratch(ctypes.byref(layer._desc), ctypes.c_void_p(x.data_ptr()),
+        desc = layer._desc if call == 0 else desc0
+        s = lib.moe_forward_static_scratch(ctypes.byref(desc), ctypes.c_void_p(x.data_ptr()),
                                            ctypes.c_void_p(out.data_ptr()), T, stream)
         assert s == gpu_lib.MOE_OK, gpu_lib.status_string(s)
         torch.cuda.synchronize()

@@ -73,6 +73,8 @@ def load(path: str | None = None):
             "moe_forward_residual": ([vp, vp, vp, vp, i, vp], st),
             "moe_forward_host": ([vp, vp, vp, i, vp], st),
             "moe_debug_expert_outputs": ([vp, vp, i, vp], st),
+            "moe_debug_route_records": ([vp, i, vp, vp, vp, vp, vp, vp, vp], st),
+            "moe_debug_hold_grid_barrier": ([vp, i, vp], st),
             "moe_rmsnorm": ([vp, vp, i, i, f, vp], st),
             "moe_quantize_nvfp4": ([vp, i, i, i, vp, vp, vp, vp], st),
             "moe_get_device_status": ([vp, vp], st),
@@ -83,6 +85,7 @@ def load(path: str | None = None):
             "moe_forward_static_scratch": ([ctypes.POINTER(MoeLayerDesc), vp, vp, i, vp], st),
             "moe_stack_create": ([ctypes.POINTER(vp), i, ctypes.POINTER(vp)], st),
             "moe_stack_forward": ([vp, vp, vp, i, f, vp, vp], st),
+            "moe_stack_forward_host": ([vp, vp, vp, i, f, vp], st),
             "moe_stack_destroy": ([vp], st),
             "moe_status_string": ([st], ctypes.c_char_p),
         }
@@ -164,11 +167,10 @@ class MoeLayer:
         self._desc = desc
 
     # -- calls ----------------------------------------------------------------
-    def route(self, x, stream=None):
-        _require_cuda(x)
-        T = x.shape[0]
-        dev = x.device
-        out = {
+    _RECORDS = ("ids", "w", "counts", "offsets", "perm", "pos")
+
+    def _records(self, T, dev):
+        return {
             "ids": torch.empty((T, self.k), dtype=torch.int32, device=dev),
             "w": torch.empty((T, self.k), dtype=torch.float32, device=dev),
             "counts": torch.empty(self.E, dtype=torch.int32, device=dev),
@@ -176,10 +178,28 @@ class MoeLayer:
             "perm": torch.empty(T * self.k, dtype=torch.int32, device=dev),
             "pos": torch.empty((T, self.k), dtype=torch.int32, device=dev),
         }
-        _check(load().moe_route(self._h, _ptr(x), T, *(_ptr(out[n]) for n in
-                                                       ("ids", "w", "counts", "offsets", "perm", "pos")),
-                                _stream(stream)), "moe_route")
+
+    def route(self, x, stream=None):
+        _require_cuda(x)
+        T = x.shape[0]
+        out = self._records(T, x.device)
+        _check(load().moe_route(self._h, _ptr(x), T, *(_ptr(out[n]) for n in self._RECORDS), _stream(stream)),
+               "moe_route")
         return out
+
+    def route_records(self, T, stream=None):
+        """The routing records the last forward (or route) of T tokens left in
+        the workspace, as that path's own kernels computed them."""
+        out = self._records(T, self.workspace.device)
+        _check(load().moe_debug_route_records(self._h, T, *(_ptr(out[n]) for n in self._RECORDS),
+                                              _stream(stream)), "moe_debug_route_records")
+        return out
+
+    def hold_grid_barrier(self, hold: bool, stream=None):
+        """Test hook: make the decode kernel's grid barriers wait for an arrival
+        that never comes (its bounded wait then runs out), or restore them."""
+        _check(load().moe_debug_hold_grid_barrier(self._h, 1 if hold else 0, _stream(stream)),
+               "moe_debug_hold_grid_barrier")
 
     def forward(self, x, out=None, res=None, stream=None):
         _require_cuda(x, out, res)
@@ -257,6 +277,13 @@ class MoeStack:
         _check(load().moe_stack_forward(self._h, _ptr(x), _ptr(out), T, float(eps), _ptr(layer_out),
                                         _stream(stream)), "moe_stack_forward")
         return out
+
+    def forward_host(self, x_host, out_host, eps=1e-6, stream=None):
+        """x_host, out_host: CPU tensors [T, d] bf16 (pinned for async copies)."""
+        T = x_host.shape[0]
+        _check(load().moe_stack_forward_host(self._h, _ptr(x_host), _ptr(out_host), T, float(eps),
+                                             _stream(stream)), "moe_stack_forward_host")
+        return out_host
 
     def close(self):
         if getattr(self, "_h", None) is not None:

@@ -125,34 +125,43 @@ moe_status forward_impl(moe_layer *ly, const uint16_t *x, const uint16_t *res, u
     }
     // Token chunks of at most tdec tokens run the streaming expert stage; a
     // chunk is a full layer forward (route, experts, combine) of its tokens.
-    const bool single = T <= tdec;
     for (int t0 = 0; t0 < T; t0 += tdec) {
         const int n = T - t0 < tdec ? T - t0 : tdec;
         const uint16_t *xc = x + (size_t)t0 * L.d;
-        if (single) prof_mark(ly, 0, st);
         cudaError_t e = launch_route_small(L, ly->ws, xc, n, st);
         ++launches;
-        if (single) prof_mark(ly, 1, st);
         if (e == cudaSuccess) e = launch_decode_gateup(L, ly->ws, xc, n, st);
         ++launches;
-        if (single) prof_mark(ly, 2, st);
         if (e == cudaSuccess) e = launch_decode_down(L, ly->ws, xc, n, st);
         ++launches;
-        if (single) prof_mark(ly, 3, st);
         if (e == cudaSuccess)
             e = launch_combine(L, ly->ws, res ? res + (size_t)t0 * L.d : nullptr, out + (size_t)t0 * L.d, n, st);
         ++launches;
-        if (single) prof_mark(ly, 4, st);
         if (e != cudaSuccess) {
             ly->last_launches = launches;
             return MOE_ERR_CUDA;
         }
     }
-    if (single && ly->prof_count < ly->prof_max) {
-        ly->prof_nk = 4;
-        ++ly->prof_count;
-    }
     ly->last_launches = launches;
+    return MOE_OK;
+}
+
+// Device-to-device copies of the routing records in the workspace (any
+// destination may be NULL).
+moe_status copy_records(const moe_layer *ly, int T, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
+                        int32_t *perm, int32_t *pos, cudaStream_t st) {
+    const LayerDev &L = ly->L;
+    const Workspace &ws = ly->ws;
+    const size_t Tk = (size_t)T * L.k;
+    struct {
+        void *dst;
+        const void *src;
+        size_t bytes;
+    } cp[] = {{ids, ws.ids, Tk * 4}, {w, ws.w, Tk * 4},          {counts, ws.counts, (size_t)L.E * 4},
+              {offsets, ws.offsets, (size_t)(L.E + 1) * 4},     {perm, ws.perm, Tk * 4}, {pos, ws.pos, Tk * 4}};
+    for (auto &c : cp)
+        if (c.dst && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+            return MOE_ERR_CUDA;
     return MOE_OK;
 }
 
@@ -225,17 +234,20 @@ moe_status moe_route(moe_layer *ly, const void *x, int T, int32_t *ids, float *w
     }
     ly->last_launches = launches;
     if (e != cudaSuccess) return MOE_ERR_CUDA;
-    const size_t Tk = (size_t)T * L.k;
-    struct {
-        void *dst;
-        const void *src;
-        size_t bytes;
-    } cp[] = {{ids, ws.ids, Tk * 4}, {w, ws.w, Tk * 4},          {counts, ws.counts, (size_t)L.E * 4},
-              {offsets, ws.offsets, (size_t)(L.E + 1) * 4},     {perm, ws.perm, Tk * 4}, {pos, ws.pos, Tk * 4}};
-    for (auto &c : cp)
-        if (c.dst && cudaMemcpyAsync(c.dst, c.src, c.bytes, cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-            return MOE_ERR_CUDA;
-    return MOE_OK;
+    return copy_records(ly, T, ids, w, counts, offsets, perm, pos, st);
+}
+
+moe_status moe_debug_route_records(moe_layer *ly, int T, int32_t *ids, float *w, int32_t *counts, int32_t *offsets,
+                                   int32_t *perm, int32_t *pos, void *stream) {
+    if (!ly || T < 1 || T > ly->L.max_T) return MOE_ERR_INVALID_ARG;
+    return copy_records(ly, T, ids, w, counts, offsets, perm, pos, (cudaStream_t)stream);
+}
+
+moe_status moe_debug_hold_grid_barrier(moe_layer *ly, int hold, void *stream) {
+    if (!ly) return MOE_ERR_INVALID_ARG;
+    static const uint32_t kOne = 1u, kZero = 0u;
+    return cuda_status(cudaMemcpyAsync(&ly->ws.ctrl->test_hold, hold ? &kOne : &kZero, sizeof(uint32_t),
+                                       cudaMemcpyHostToDevice, (cudaStream_t)stream));
 }
 
 moe_status moe_forward(moe_layer *ly, const void *x, void *out, int T, void *stream) {
@@ -365,6 +377,20 @@ moe_status moe_stack_forward(moe_stack *sk, const void *x, void *out, int T, flo
     ly->last_launches = 1;
     if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) return MOE_ERR_UNSUPPORTED;
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+moe_status moe_stack_forward_host(moe_stack *sk, const void *x_host, void *out_host, int T, float eps,
+                                  void *stream) {
+    if (!sk || !x_host || !out_host || T < 1 || T > 8 || T > sk->first->L.max_T || !(eps >= 0.f))
+        return MOE_ERR_INVALID_ARG;
+    moe_layer *ly = sk->first;
+    cudaStream_t st = (cudaStream_t)stream;
+    const size_t bytes = (size_t)T * ly->L.d * 2;
+    if (cudaMemcpyAsync(ly->ws.xbuf, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess) return MOE_ERR_CUDA;
+    const moe_status s = moe_stack_forward(sk, ly->ws.xbuf, ly->ws.obuf, T, eps, nullptr, stream);
+    if (s != MOE_OK) return s;
+    if (cudaMemcpyAsync(out_host, ly->ws.obuf, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess) return MOE_ERR_CUDA;
+    return cuda_status(cudaStreamSynchronize(st));
 }
 
 moe_status moe_stack_destroy(moe_stack *sk) {

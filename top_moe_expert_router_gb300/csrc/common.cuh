@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "moe.h"
 
 namespace moe {
@@ -35,7 +37,8 @@ struct Control {
     int32_t n_uniq;          // number of experts with at least one token
     int32_t n_tiles_gu;      // prefill: gate/up tiles
     int32_t n_tiles_dn;      // prefill: down tiles
-    uint32_t pad0[27];
+    uint32_t test_hold;      // test hook: arrivals the decode kernel's grid barriers wait for beyond the grid (0)
+    uint32_t pad0[26];
     CtrLine grid_bar;        // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
     CtrLine grid_exit;       // fused decode kernel: CTAs that finished
     CtrLine h_ready[2];      // fused decode kernel: h rows written, first / second half of the experts
@@ -89,6 +92,20 @@ struct Workspace {
 };
 
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+// cudaFuncSetAttribute(MaxDynamicSharedMemorySize) applies to the current
+// device only: `done` records, per device ordinal (< 64), where it was set,
+// so that one process driving several GPUs sets it on each.
+inline cudaError_t set_smem_limit_once(const void *func, int bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? 1ull << dev : 0ull;
+    if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+    return e;
+}
 
 // Computes the layout; with base == nullptr only the size is meaningful.
 inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int max_T) {

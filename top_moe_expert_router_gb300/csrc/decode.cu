@@ -1,14 +1,14 @@
-// decode.cu — expert stage for small batches (decode / speculative verify,
-// T <= 16): the active experts' weights are streamed from HBM exactly once
-// through a ring of shared-memory stages filled by bulk TMA copies, and the
-// FFN arithmetic runs on CUDA cores with fp32 accumulation.
+// decode.cu — the split streaming expert stage (two launches per chunk of at
+// most 16 tokens), used for NVFP4 batches of more than 16 tokens, which the
+// bf16 grouped GEMMs of the prefill path do not take. The single-launch layer
+// kernel (decode_fused.cuh) covers every batch of at most 16 tokens.
 //
-// Decode is bound by streaming weights from HBM, not by matmul speed, and
-// fetching weights ahead of the compute that needs them hides the wait ("How
-// SGLang-TorchTPU accelerated an 816B-parameter MoE on TPU v7", sections
-// "Introduction" and "Key optimisations"). With at most 16 tokens, an expert
-// sees about one token per step, so each weight element feeds 1-2 FMAs: the
-// tensor cores would idle, and the work is a memory stream.
+// Decode-sized chunks are bound by streaming weights from HBM, not by matmul
+// speed, and fetching weights ahead of the compute that needs them hides the
+// wait ("How SGLang-TorchTPU accelerated an 816B-parameter MoE on TPU v7",
+// sections "Introduction" and "Key optimisations"). With at most 16 tokens
+// per chunk an expert sees about one token, so each weight element feeds 1-2
+// FMAs and the work is a memory stream.
 //
 // Two persistent kernels, grid = one CTA per SM:
 //   gate/up:  h[r, i] = silu(Wg[e,i,:] . x_t) * (Wu[e,i,:] . x_t)   (fp32)
@@ -443,13 +443,9 @@ static cudaError_t launch_gateup_t(const LayerDev &L, const DecodeArgs &a0, cuda
     if (fixed + 2 * stage > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
     const int ns = (int)((kSmemBudget - fixed) / stage);
     pick_stages(ns, a);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_gateup_kernel<TM, FP4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    const cudaError_t e = set_smem_limit_once((const void *)decode_gateup_kernel<TM, FP4>, kSmemBudget, attr_set);
+    if (e != cudaSuccess) return e;
     return launch_pdl(decode_gateup_kernel<TM, FP4>, L.num_sms, kDecodeThreads, fixed + (size_t)a.nstages * stage,
                       st, a);
 }
@@ -462,13 +458,9 @@ static cudaError_t launch_down_t(const LayerDev &L, const DecodeArgs &a0, cudaSt
     if (fixed + 2 * stage > (size_t)kSmemBudget) return cudaErrorInvalidConfiguration;
     const int ns = (int)((kSmemBudget - fixed) / stage);
     pick_stages(ns, a);
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_down_kernel<TM, FP4>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    const cudaError_t e = set_smem_limit_once((const void *)decode_down_kernel<TM, FP4>, kSmemBudget, attr_set);
+    if (e != cudaSuccess) return e;
     return launch_pdl(decode_down_kernel<TM, FP4>, L.num_sms, kDecodeThreads, fixed + (size_t)a.nstages * stage, st,
                       a);
 }

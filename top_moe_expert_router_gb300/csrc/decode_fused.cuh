@@ -111,11 +111,15 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
 }
 
 // Grid barrier over all CTAs of the (cooperative) launch: arrival counter
-// `target` = (barrier index) x (grid size). Bounded wait.
-__device__ inline bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, volatile int *abort_flag) {
+// `target` = (barrier index) x (grid size), plus *hold, a test hook that is 0
+// in normal operation (nonzero: an arrival that never comes, so the bounded
+// wait runs out). Bounded wait.
+__device__ inline bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, volatile int *abort_flag,
+                                    const uint32_t *hold) {
     __syncthreads();
     __shared__ int ok;
     if (threadIdx.x == 0) {
+        target += *reinterpret_cast<const volatile uint32_t *>(hold);
         fence_acq_rel_gpu();
         atomicAdd(ctr, 1u);
         ok = 1;
@@ -802,7 +806,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
         }
         if (!x_ready) mbar_wait_or_abort(xbar, 0, err, abort_flag);  // CTAs without router rows
     }
-    grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 1) * G, err, abort_flag);
+    grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 1) * G, err, abort_flag, &ctrl->test_hold);
 
     if (FP4 && x_bytes) {
         // NVFP4 gate/up sums in fp16: keep the staged tokens as fp16(x / max|x|)
@@ -1289,7 +1293,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
             hbase[0] += (uint32_t)(U1 * I);
             hbase[1] += (uint32_t)((n_uniq - U1) * I);
         }
-        grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 2) * G, err, abort_flag);
+        grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 2) * G, err, abort_flag, &ctrl->test_hold);
     }
     }  // layers
     // ---- exit: the last CTA out resets the grid-barrier counters ----
@@ -1355,13 +1359,9 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     a.x_router_ring = !a.x_in_smem && (size_t)a.nslots * a.slot_bytes >= (size_t)T * L.d * 2 ? 1 : 0;
     a.nprod = a.nslots % 4 == 0 ? 4 : (a.nslots % 2 == 0 ? 2 : 1);
     const size_t smem = fixed + xb2 + (size_t)a.nslots * a.slot_bytes;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(decode_layer_kernel<TM, FP4, STACK>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = set_smem_limit_once((const void *)decode_layer_kernel<TM, FP4, STACK>, kSmemBudget, attr_set);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(L.num_sms);
     cfg.blockDim = dim3(Warps<TM, FP4>::kThreads);

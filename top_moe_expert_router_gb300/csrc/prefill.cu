@@ -382,13 +382,9 @@ bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K
 template <int EPI, bool SPLIT_B>
 static cudaError_t launch_gemm(const CUtensorMap &a, const CUtensorMap &b, const CUtensorMap &b2,
                                const GemmParams &p, int grid, cudaStream_t st) {
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(grouped_gemm_kernel<EPI, SPLIT_B>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> attr_set{0};
+    cudaError_t e = set_smem_limit_once((const void *)grouped_gemm_kernel<EPI, SPLIT_B>, (int)kGemmSmem, attr_set);
+    if (e != cudaSuccess) return e;
     grouped_gemm_kernel<EPI, SPLIT_B><<<grid, kGemmThreads, kGemmSmem, st>>>(a, b, b2, p);
     return cudaGetLastError();
 }

@@ -21,23 +21,24 @@ using namespace moe;
 // Scratch of the static-scratch forward, shared by every call on a device.
 static __device__ __align__(256) unsigned char g_static_scratch[MOE_STATIC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-void *g_scratch_ptr[kMaxDevices];  // device address of g_static_scratch, per device
-int g_num_sms[kMaxDevices];
-
 bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
 
-// One-time set-up per device, with that device current: the host-side name
-// g_static_scratch is only a stand-in, so the kernels get the device address.
-moe_status device_setup(int dev) {
-    if (dev < 0 || dev >= kMaxDevices) return MOE_ERR_UNSUPPORTED;
-    if (g_scratch_ptr[dev]) return MOE_OK;
+// Set-up, done on every call with the caller's device and context current:
+// the host-side name g_static_scratch is only a stand-in, so the kernel gets
+// the array's device address in the current context (a lookup, no
+// allocation). Nothing is cached, so a context created later (after
+// cudaDeviceReset, or the caller's own context on the same device) gets its
+// own module's address, and concurrent host threads share no state.
+moe_status device_setup(void **scratch, int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     void *ptr = nullptr;
     if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr) return MOE_ERR_CUDA;
     int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
-    g_num_sms[dev] = sms;
-    g_scratch_ptr[dev] = ptr;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return MOE_ERR_CUDA;
+    *scratch = ptr;
+    *num_sms = sms;
     return MOE_OK;
 }
 
@@ -45,8 +46,13 @@ moe_status device_setup(int dev) {
 
 extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, const void *x, void *out, int T,
                                                  void *stream) {
+    if (!desc) return MOE_ERR_INVALID_ARG;
+    // the shape checks of a layer sized for exactly T tokens (desc->max_tokens
+    // is not used); no GPU work
+    moe_layer_desc shape = *desc;
+    shape.max_tokens = T < 1 ? 1 : T;
     size_t ignore = 0;
-    moe_status s = moe_workspace_size(desc, &ignore);  // shape checks only, no GPU work
+    moe_status s = moe_workspace_size(&shape, &ignore);
     if (s != MOE_OK) return s;
     if (!x || !out || !aligned16(x) || !aligned16(out) || x == out || T < 1 || T > 16 || !desc->w_router ||
         !aligned16(desc->w_router))
@@ -61,14 +67,14 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
         for (const void *q : p)
             if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
     }
-    // the tokens' rows sit in shared memory next to a ring of at least two stages
-    if ((size_t)T * desc->d * 2 + 2 * (4 * (size_t)desc->d * 2) + 4096 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
     const Workspace need = workspace_layout(nullptr, desc->d, desc->E, desc->top_k, desc->I, T);
     if (need.bytes > MOE_STATIC_SCRATCH_BYTES) return MOE_ERR_UNSUPPORTED;
+    // the tokens' rows sit in shared memory next to a ring of at least two stages
+    if ((size_t)T * desc->d * 2 + 2 * (4 * (size_t)desc->d * 2) + 4096 > 227 * 1024) return MOE_ERR_UNSUPPORTED;
 
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
-    s = device_setup(dev);
+    void *scratch = nullptr;
+    int num_sms = 0;
+    s = device_setup(&scratch, &num_sms);
     if (s != MOE_OK) return s;
 
     LayerDev L{};
@@ -92,9 +98,9 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
     L.gg = desc->g_gate;
     L.gu = desc->g_up;
     L.gd = desc->g_down;
-    L.num_sms = g_num_sms[dev];
+    L.num_sms = num_sms;
     L.expert_norm = desc->expert_out_norm ? 1 : 0;
-    const Workspace ws = workspace_layout(g_scratch_ptr[dev], L.d, L.E, L.k, L.I, T);
+    const Workspace ws = workspace_layout(scratch, L.d, L.E, L.k, L.I, T);
 
     cudaStream_t st = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the control words (error
