@@ -4,11 +4,12 @@
 A step is one pass of the whole layer (router, softmax/top-8/renormalise,
 permutation, expert SwiGLU FFNs, weighted combine) over one batch of
 synthetic tokens, with the weights resident in HBM. The default run measures
-all five workloads of the layer (d=4096, E=256 experts, top-8, I=1536):
+all six workloads of the layer (d=4096, E=256 experts, top-8, I=1536):
 
   decode_t1        T=1 single-request decode, bf16 experts      (the headline)
   decode_t4/_t16   T=4 / 16 batched decode / speculative verify, bf16 experts
   prefill_t4096    T=4096 prefill, bf16 experts, Zipf-skewed router bias
+  nvfp4_prefill_t4096  the same prefill layer with NVFP4 experts
   nvfp4_stack_t4   8 stacked layers (RMSNorm, MoE, residual), T=4, NVFP4 experts
 
 and prints ONE JSON line: the headline's fields at the top level and every
@@ -46,7 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLUSH_BYTES = 256 << 20
 POOL = 64
 HEADLINE = "decode_t1"
-ORDER = ["decode_t1", "decode_t4", "decode_t16", "prefill_t4096", "nvfp4_stack_t4"]
+ORDER = ["decode_t1", "decode_t4", "decode_t16", "prefill_t4096", "nvfp4_prefill_t4096", "nvfp4_stack_t4"]
 
 
 # ---------------------------------------------------------------------------
@@ -246,10 +247,28 @@ def oracle_decode_rates(w, wr, bias, pool_np, budget_s=4.0):
     return line
 
 
+def oracle_nvfp4_packs(w, layer, need):
+    """The oracle's own NVFP4 quantisation of the listed experts of one layer
+    (full-shape arrays, other experts left zero)."""
+    import oracle
+    g, u, d = datagen.expert_weights(w, layer, experts=need)
+    host = {}
+    for name, arr in (("gate", g), ("up", u), ("down", d)):
+        E, rows, K = arr.shape
+        q = np.zeros((E, rows, K // 2), np.uint8)
+        s = np.zeros((E, rows, K // 16), np.uint8)
+        gs = np.ones(E, np.float32)
+        for e in need:
+            q[e], s[e], gs[e] = oracle.quantize_nvfp4(arr[e])
+        host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
+    return host
+
+
 def oracle_prefill_rates(w, wr, bias, x, sample_all=256, sample_one=8):
     """Prefill: routing of all T tokens plus the expert FFNs of a seeded token
-    sample, extrapolated per token to T (all threads: 256 tokens; one thread:
-    8 tokens)."""
+    sample, extrapolated per token to T (all threads: sample_all tokens; one
+    thread: sample_one tokens). NVFP4 experts: the oracle quantises the
+    sample's experts itself, untimed."""
     import oracle
     cores = oracle.max_threads()
     lg = oracle.router_logits(x, wr, bias)
@@ -257,8 +276,11 @@ def oracle_prefill_rates(w, wr, bias, x, sample_all=256, sample_one=8):
     rng = np.random.default_rng(1)
     sample = np.sort(rng.choice(w.T, sample_all, replace=False))
     need = np.unique(ids[sample])
-    g, u, d = datagen.expert_weights(w, experts=need)
-    L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
+    if w.fmt == "nvfp4":
+        L = oracle.Layer(wr, k=w.k, nvfp4=oracle_nvfp4_packs(w, 0, need), router_bias=bias)
+    else:
+        g, u, d = datagen.expert_weights(w, experts=need)
+        L = oracle.Layer(wr, g, u, d, router_bias=bias, k=w.k)
     out = {}
     for threads, n_s in ((cores, sample_all), (1, sample_one)):
         oracle.set_threads(threads)
@@ -291,18 +313,7 @@ def oracle_stack_rates(w, x_batch, n_one=1):
         wr = datagen.router_weights(w, li)
         u_in = oracle.rmsnorm(cur, 1e-6)
         ids, _, _ = oracle.select_topk(oracle.router_logits(u_in, wr), w.k)
-        need = np.unique(ids)
-        g, u, d = datagen.expert_weights(w, li, experts=need)
-        host = {}
-        for name, arr in (("gate", g), ("up", u), ("down", d)):
-            E, rows, K = arr.shape
-            q = np.zeros((E, rows, K // 2), np.uint8)
-            s = np.zeros((E, rows, K // 16), np.uint8)
-            gs = np.ones(E, np.float32)
-            for e in need:
-                q[e], s[e], gs[e] = oracle.quantize_nvfp4(arr[e])
-            host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
-        L = oracle.Layer(wr, k=w.k, nvfp4=host)
+        L = oracle.Layer(wr, k=w.k, nvfp4=oracle_nvfp4_packs(w, li, np.unique(ids)))
         cur = oracle.residual_add(cur, L.forward(u_in)["y"])
         packs.append(L)
         routers.append(wr)
@@ -426,11 +437,12 @@ def e2e_host(ctx, w, pool_np, call, n_steps):
     import torch
     xh = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16).pin_memory() for p in pool_np]
     oh = torch.empty((w.T, w.d), dtype=torch.bfloat16).pin_memory()
+    n = len(xh)
     for s in range(3):
-        call(xh[s % POOL], oh)
+        call(xh[s % n], oh)
     t0 = time.perf_counter()
     for s in range(n_steps):
-        call(xh[s % POOL], oh)
+        call(xh[s % n], oh)
     dt = time.perf_counter() - t0
     v, _ = aggregate(w.T * n_steps, dt, ctx.dist, ctx.device)
     return {"value": v, "unit": "tok/s", "h2d_bytes_per_step": w.T * w.d * 2, "d2h_bytes_per_step": w.T * w.d * 2,
@@ -494,18 +506,28 @@ def measure_prefill(ctx, w, gl, host):
     ex_ms = prof[:, 1].astype(np.float64)
     tf = flops / (ex_ms.mean() / 1e3) / 1e12
     peak_tf = ctx.peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])
-    wbytes = float(U.mean()) * w.expert_bytes_bf16
+    fp4 = w.fmt == "nvfp4"
+    wbytes = float(U.mean()) * (w.expert_bytes_nvfp4 if fp4 else w.expert_bytes_bf16)
     gbs = wbytes / (ex_ms.mean() / 1e3) / 1e9
     hbm = ctx.peaks["hbm_gbs"]
-    # at T = 4096 the expert GEMMs' weight stream outlasts their arithmetic
-    # (128 FLOP/B < the ridge point), so HBM is the binding ceiling
-    roof = {"kernel": "grouped_gemm_kernel (gate/up + down)", "bound": "hbm", "achieved": gbs, "peak": hbm,
-            "unit": "GB/s", "frac": gbs / hbm, "traffic": None, "peak_source": ctx.peak_src,
-            "bytes_per_launch": wbytes, "bytes_rule": "unique active experts x 3*d*I*2 B (weights read once)",
-            "ms_per_launch": float(ex_ms.mean()),
-            "tensor": {"achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf,
-                       "flops_per_launch": flops,
-                       "ceiling_frac": (flops / peak_tf / 1e12) / max(flops / peak_tf / 1e12, wbytes / hbm / 1e9)}}
+    t_flop, t_byte = flops / peak_tf / 1e12, wbytes / hbm / 1e9
+    tensor = {"achieved": tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": tf / peak_tf, "flops_per_launch": flops,
+              "peak_note": "16-bit dense tensor peak (f16 and bf16 run at the same rate)",
+              "ceiling_frac": t_flop / max(t_flop, t_byte)}
+    hbm_obj = {"achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "bytes_per_launch": wbytes,
+               "bytes_rule": ("unique active experts x " + ("10,616,832 B (NVFP4 codes + block scales)" if fp4
+                                                           else "3*d*I*2 B") + " (weights read once)")}
+    kname = ("grouped_gemm_fp4_kernel (gate/up + down, NVFP4 tiles widened in shared memory)" if fp4
+             else "grouped_gemm_kernel (gate/up + down)")
+    if t_byte > t_flop:
+        # bf16 at T = 4096: the weight stream outlasts the arithmetic (128
+        # FLOP/B < the ridge point), so HBM is the binding ceiling
+        roof = dict(hbm_obj, kernel=kname, bound="hbm", traffic=None, peak_source=ctx.peak_src,
+                    ms_per_launch=float(ex_ms.mean()), tensor=tensor)
+    else:
+        # NVFP4 weights are 3.55x fewer bytes: the tensor pipe is the ceiling
+        roof = dict(tensor, kernel=kname, bound="tensor", traffic=None, peak_source=ctx.peak_src,
+                    ms_per_launch=float(ex_ms.mean()), hbm=hbm_obj)
     kernel_ms = {"route_gather": float(prof[:, 0].mean()), "expert_gemms": float(ex_ms.mean()),
                  "combine": float(prof[:, 2].mean())}
     res = {"value": value, "unit": "tok/s", "steps": args.steps, "warmup": args.warmup,
@@ -513,10 +535,13 @@ def measure_prefill(ctx, w, gl, host):
            "gpu_launches": launches, "clocks": clk,
            "config": workload_config(w, tokens=f"pool of {n_pool} seeded 4096-token batches",
                                      l2="flushed before every step (256 MiB write), outside the step events")}
+    if fp4:
+        res["dtype"] = "nvfp4 experts widened to f16/bf16 in shared memory, fp32 accumulate"
     res["e2e"] = e2e_host(ctx, w, pool_np, gl.forward_host, min(args.e2e_steps, args.steps, 20))
     if ctx.rank == 0 and not args.no_cpu_baseline:
         wr, bias = host
-        res["cpu_baseline"] = oracle_prefill_rates(w, wr, bias, pool_np[0])
+        res["cpu_baseline"] = (oracle_prefill_rates(w, wr, bias, pool_np[0], 64, 4) if fp4
+                               else oracle_prefill_rates(w, wr, bias, pool_np[0]))
     return res
 
 
@@ -608,10 +633,11 @@ def run_ours(args):
     results = {}
 
     bf16_names = [n for n in names if datagen.WORKLOADS[n].fmt == "bf16"]
-    if bf16_names:
+    fp4_prefill = [n for n in names if datagen.WORKLOADS[n].fmt == "nvfp4" and datagen.WORKLOADS[n].layers == 1]
+    if bf16_names or fp4_prefill:
         # decode and prefill share the layer's weights (seed 0, layer 0);
         # prefill adds the skewed router bias
-        w0 = datagen.WORKLOADS[bf16_names[0]]
+        w0 = datagen.WORKLOADS[(bf16_names + fp4_prefill)[0]]
         if args.experts:
             w0 = dataclasses.replace(w0, E=args.experts)
         wr = datagen.router_weights(w0)
@@ -630,11 +656,26 @@ def run_ours(args):
             results[n] = fn(ctx, w, gl, (wr, bias))
             gl.close()
             torch.cuda.empty_cache()
+        for n in fp4_prefill:
+            # the same layer's experts quantised to NVFP4 on the GPU (set-up, not timed)
+            w = datagen.WORKLOADS[n]
+            if args.experts:
+                w = dataclasses.replace(w, E=args.experts)
+            packs = {}
+            for name in ("gate", "up", "down"):
+                packs["q_" + name], packs["s_" + name], packs["g_" + name] = moe.quantize_nvfp4(dev[name])
+            bias = datagen.router_bias(w)
+            gl = moe.MoeLayer(dev["wr"], nvfp4=packs, router_bias=torch.from_numpy(bias).to(device),
+                              top_k=w.k, max_tokens=w.T)
+            results[n] = measure_prefill(ctx, w, gl, (wr, bias))
+            gl.close()
+            del packs
+            torch.cuda.empty_cache()
         del dev
         torch.cuda.empty_cache()
     for n in names:
         w = datagen.WORKLOADS[n]
-        if w.fmt == "nvfp4":
+        if w.fmt == "nvfp4" and w.layers > 1:
             if args.experts:
                 w = dataclasses.replace(w, E=args.experts)
             layers = build_stack(ctx, w)

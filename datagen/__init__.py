@@ -161,6 +161,9 @@ WORKLOADS = {
                               router_scale=ROUTER_SCALE_D4096, zipf_alpha=ZIPF_ALPHA),
     "nvfp4_stack_t4": Workload("nvfp4_stack_t4", T=4, d=4096, E=256, k=8, I=1536,
                                fmt="nvfp4", router_scale=ROUTER_SCALE_D4096, layers=8),
+    # the prefill layer (same seeded weights and router bias) with its experts in NVFP4
+    "nvfp4_prefill_t4096": Workload("nvfp4_prefill_t4096", T=4096, d=4096, E=256, k=8, I=1536, fmt="nvfp4",
+                                    router_scale=ROUTER_SCALE_D4096, zipf_alpha=ZIPF_ALPHA),
 }
 
 

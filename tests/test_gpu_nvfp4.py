@@ -54,8 +54,10 @@ def _quantize_on_gpu(moe, g, u, d):
     return packs
 
 
-@pytest.mark.parametrize("T", [1, 4, 16, 17, 40])
+@pytest.mark.parametrize("T", [1, 4, 16, 17, 40, 300])
 def test_small_nvfp4_layer(gpu_lib, T):
+    """T <= 16: the single-launch decode kernel; T > 16: the NVFP4 grouped
+    GEMMs (several 128-row tiles per expert and ragged tails at T = 300)."""
     w = datagen.Workload("fp4small", T=T, d=512, E=64, k=8, I=256, fmt="nvfp4", router_scale=4.0)
     wr = datagen.router_weights(w)
     g, u, d = datagen.expert_weights(w)
@@ -67,29 +69,75 @@ def test_small_nvfp4_layer(gpu_lib, T):
         np.testing.assert_array_equal(packs["s_" + name].cpu().numpy(), s)
         np.testing.assert_array_equal(packs["g_" + name].cpu().numpy(), gs)
         host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
-    gl = _nvfp4_gpu_layer(gpu_lib, wr, None, packs, w.k, 64)
+    gl = _nvfp4_gpu_layer(gpu_lib, wr, None, packs, w.k, 512)
     L = oracle.Layer(wr, k=w.k, nvfp4=host)
     x = datagen.tokens(w, T, start_row=3)
     xd = to_dev_bf16(x)
     r = gl.route(xd)
     y = gl.forward(xd)
-    # the forward's own routing records (a single decode launch for T <= 16)
-    rec = gl.route_records(T) if T <= 16 else None
-    Y = gl.expert_outputs(T) if T <= 16 else None
+    rec = gl.route_records(T)          # the records the forward's own kernels computed
+    Y = gl.expert_outputs(T)
     torch.cuda.synchronize()
     assert gl.device_status() == 0
-    ref = L.forward(x, forced_ids=r["ids"].cpu().numpy(), want_Y=T <= 16)
+    assert gl.last_launch_count() == (1 if T <= 16 else 7)
+    ref = L.forward(x, forced_ids=r["ids"].cpu().numpy(), want_Y=True)
     own = L.forward(x)
     check_route(r, own["ids"], own["w"], own["gap"], w.E)
-    if rec is not None:
-        check_route(rec, own["ids"], own["w"], own["gap"], w.E)
+    check_route(rec, own["ids"], own["w"], own["gap"], w.E)
     err = normwise_rel_err(datagen.bf16_to_f32(bf16_host(y)), ref["y"])
     assert err.max() <= NVFP4_TOL
-    assert err.max() < 1e-2            # the kernel adds only fp32 rounding to the shared quantisation
-    if Y is not None:
-        pos = r["pos"].cpu().numpy()
-        eY = normwise_rel_err(Y.cpu().numpy()[pos], ref["Y"])
-        assert eY.max() < 1e-2
+    # the kernels add only fp32 (decode) or bf16 h / bf16 expert-output (GEMM)
+    # rounding to the shared quantisation
+    assert err.max() < 1e-2
+    pos = r["pos"].cpu().numpy()
+    eY = normwise_rel_err(Y.cpu().numpy()[pos], ref["Y"])
+    assert eY.max() < 1e-2
+
+
+def test_nvfp4_prefill_full_size(gpu_lib):
+    """T=4096 prefill with NVFP4 experts at full size (d=4096, E=256, I=1536,
+    the skewed router bias of the bf16 prefill workload): routing bit-exact on
+    all 4096 tokens off near-ties (the route call and the forward's own
+    records), the layer output and all 8 slots of a seeded 256-token sample
+    within the NVFP4 tolerance of the oracle run on its own quantisation."""
+    w = datagen.WORKLOADS["nvfp4_prefill_t4096"]
+    T = w.T
+    wr = datagen.router_weights(w)
+    bias = datagen.router_bias(w)
+    g, u, d = datagen.expert_weights(w)
+    packs = _quantize_on_gpu(gpu_lib, g, u, d)
+    gl = _nvfp4_gpu_layer(gpu_lib, wr, bias, packs, w.k, T)
+    x = datagen.tokens(w, T)
+    xd = to_dev_bf16(x)
+    r = gl.route(xd)
+    y = gl.forward(xd)
+    rec = gl.route_records(T)
+    torch.cuda.synchronize()
+    assert gl.device_status() == 0
+    lg = oracle.router_logits(x, wr, bias)
+    ids, wts, gap = oracle.select_topk(lg, w.k)
+    check_route(r, ids, wts, gap, w.E)
+    check_route(rec, ids, wts, gap, w.E)
+    sample = np.sort(np.random.default_rng(1).choice(T, 256, replace=False))
+    gpu_ids = r["ids"].cpu().numpy()
+    need = np.unique(gpu_ids[sample])
+    host = {}
+    for name, arr in (("gate", g), ("up", u), ("down", d)):
+        q, s, gs = _quant_host(arr, need)
+        np.testing.assert_array_equal(packs["q_" + name][need].cpu().numpy(), q[need])
+        np.testing.assert_array_equal(packs["s_" + name][need].cpu().numpy(), s[need])
+        np.testing.assert_array_equal(packs["g_" + name][need].cpu().numpy(), gs[need])
+        host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
+    del g, u, d
+    L = oracle.Layer(wr, k=w.k, nvfp4=host, router_bias=bias)
+    ref = L.forward(x, tokens=sample, forced_ids=gpu_ids, want_Y=True)
+    err = normwise_rel_err(datagen.bf16_to_f32(bf16_host(y))[sample], ref["y"])
+    assert err.max() <= NVFP4_TOL and err.max() < 1e-2
+    Y = gl.expert_outputs(T)
+    pos = r["pos"].cpu().numpy()[sample]
+    Yg = Y[torch.from_numpy(pos.reshape(-1)).to(Y.device)].cpu().numpy().reshape(len(sample), w.k, -1)
+    del Y
+    assert normwise_rel_err(Yg, ref["Y"]).max() <= NVFP4_TOL
 
 
 def test_stacked_nvfp4_decode_full_size(gpu_lib):

@@ -73,9 +73,9 @@ void prof_mark(moe_layer *ly, int i, cudaStream_t st) {
         cudaEventRecord(ly->prof_events[(size_t)ly->prof_count * kProfSlots + i], st);
 }
 
-// The tensor-core grouped GEMMs take bf16 experts with d a multiple of 256
-// (down-projection N tile) and I a multiple of 128 (gate/up N tile).
-bool prefill_supported(const LayerDev &L) { return L.fmt == MOE_W_BF16 && L.d % 256 == 0 && L.I % 128 == 0; }
+// The tensor-core grouped GEMMs (bf16 or NVFP4 experts) take d a multiple of
+// 256 (down-projection N tile) and I a multiple of 128 (gate/up N tile).
+bool prefill_supported(const LayerDev &L) { return L.d % 256 == 0 && L.I % 128 == 0; }
 
 // Large-batch forward: tensor-core router, top-k, permutation, row gather,
 // grouped gate/up GEMM with SwiGLU, grouped down GEMM, combine.
@@ -84,11 +84,14 @@ moe_status forward_prefill(moe_layer *ly, const uint16_t *x, const uint16_t *res
     const LayerDev &L = ly->L;
     int launches = 0;
     prof_mark(ly, 0, st);
+    const bool fp4 = L.fmt == MOE_W_NVFP4;
     cudaError_t e = launch_route_large(L, ly->ws, x, T, st, &launches);
-    if (e == cudaSuccess) e = launch_gather_rows(L, ly->ws, x, T, st);
+    if (e == cudaSuccess) e = fp4 ? launch_gather_rows_f16(L, ly->ws, x, T, st) : launch_gather_rows(L, ly->ws, x, T, st);
     ++launches;
     prof_mark(ly, 1, st);
-    if (e == cudaSuccess) e = launch_prefill_experts(L, ly->ws, x, T, st, &launches);
+    if (e == cudaSuccess)
+        e = fp4 ? launch_prefill_experts_fp4(L, ly->ws, T, st, &launches)
+                : launch_prefill_experts(L, ly->ws, x, T, st, &launches);
     prof_mark(ly, 2, st);
     const bool y_bf16 = !L.expert_norm;  // the down GEMM's bf16 expert outputs
     if (e == cudaSuccess) e = launch_combine(L, ly->ws, res, out, T, st, y_bf16);

@@ -85,7 +85,8 @@ struct Workspace {
     uint16_t *obuf;     // [max_T, d] bf16 staging
     float *h;           // [max_T*k, I] fp32 (decode) / bf16 (prefill)
     float *Y;           // [max_T*k, d] fp32 expert outputs
-    uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill)
+    uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill; f16 for NVFP4 experts)
+    float *row_scale;   // [max_T*k] NVFP4 prefill: power-of-two scale of each gathered row
     int32_t *chunk_base;  // [ceil(max_T/kRouteChunk), E] per-chunk counts, then each chunk's first row per expert
     uint32_t *chunk_bm;   // [ceil(max_T/kRouteChunk), E] token bitmaps of each kRouteChunk-token chunk
     size_t bytes;
@@ -133,6 +134,7 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     ws.h = (float *)take(sizeof(float) * Tk * I);
     ws.Y = (float *)take(sizeof(float) * Tk * d);
     ws.xperm = (uint16_t *)take(sizeof(uint16_t) * Tk * d);
+    ws.row_scale = (float *)take(sizeof(float) * Tk);
     const size_t nchunks = ((size_t)max_T + kRouteChunk - 1) / kRouteChunk;
     ws.chunk_base = (int32_t *)take(sizeof(int32_t) * nchunks * E);
     ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E);
@@ -393,5 +395,9 @@ cudaError_t launch_gather_rows(const LayerDev &L, const Workspace &ws, const uin
 cudaError_t launch_router_gemm(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
 cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
                                    int *launches);
+// prefill_fp4.cu
+cudaError_t launch_gather_rows_f16(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
+cudaError_t launch_prefill_experts_fp4(const LayerDev &L, const Workspace &ws, int T, cudaStream_t st,
+                                       int *launches);
 
 }  // namespace moe

@@ -22,150 +22,16 @@
 #include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
-#include "common.cuh"
+#include "gemm.cuh"
 
 namespace moe {
 
-constexpr int BM = 128, BK = 64, BN = 256;
 constexpr int kGemmStages = 4;
 constexpr int kGemmThreads = 192;
-constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kABytes = BM * BK * 2;       // 16 KB
 constexpr uint32_t kBBytes = BN * BK * 2;       // 32 KB
 constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr size_t kGemmSmem = 1024 + (size_t)kGemmStages * kStageBytes + 256;
-
-enum { EPI_LOGITS = 0, EPI_SWIGLU = 1, EPI_F32 = 2, EPI_BF16 = 3 };
-
-struct GemmParams {
-    const int32_t *tile_off;  // [G+1] prefix of 128-row tiles per group; nullptr: one group
-    const int32_t *row_off;   // [G+1] first row of each group in A and in the output
-    int n_rows;               // rows of the single group (tile_off == nullptr)
-    int groups;
-    int nt;                   // n-tiles per m-tile
-    int K;
-    int b_rows_per_group;     // rows of B per group (0 for the router)
-    float *out_f32;           // logits [rows, ld] / Y [rows, ld]
-    uint16_t *out_bf16;       // H [rows, ld] (SwiGLU) / Y [rows, ld] (EPI_BF16)
-    int ld;                   // output row stride in elements
-    int n_valid;              // columns < n_valid are stored (router: E)
-    const float *bias;
-    uint32_t *err;
-    int ksplit;               // single group only: K split in ksplit parts, part s written at out_f32 + s * split_stride
-    size_t split_stride;
-};
-
-// ---------------------------------------------------------------------------
-// PTX wrappers: TMA tensor loads, tcgen05 (TMEM alloc, MMA, commit, ld)
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, int x, int y, uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(tm)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-__device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
-                                         uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void mma_commit(uint64_t *bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t v[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
-        "%15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
-          "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-}
-
-__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major tile written by TMA with the
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((addr & 0x3FFFFu) >> 4);   // start address
-    d |= (uint64_t)1 << 16;                    // leading byte offset (unused with this swizzle)
-    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                    // descriptor version
-    d |= (uint64_t)2 << 61;                    // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor: kind::f16 with bf16 A and B, fp32 accumulator,
-// both operands K-major, M = 128, N = 256.
-constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
-                            ((uint32_t)(BM >> 4) << 24);
-
-// ---------------------------------------------------------------------------
-// tile scheduling
-// ---------------------------------------------------------------------------
-struct TileInfo {
-    int g, m, n, row0, rows, ks;
-};
-
-__device__ __forceinline__ int total_tiles(const GemmParams &p) {
-    if (!p.tile_off) return ((p.n_rows + BM - 1) / BM) * p.nt * p.ksplit;
-    return p.tile_off[p.groups] * p.nt;
-}
-
-__device__ __forceinline__ TileInfo tile_info(const GemmParams &p, int tile) {
-    TileInfo ti;
-    if (!p.tile_off) {
-        const int mt = (p.n_rows + BM - 1) / BM;
-        ti.g = 0;
-        ti.m = tile % mt;
-        ti.n = (tile / mt) % p.nt;
-        ti.ks = tile / (mt * p.nt);
-        ti.row0 = 0;
-        ti.rows = p.n_rows;
-        return ti;
-    }
-    int lo = 0, hi = p.groups;  // find g: tile_off[g]*nt <= tile < tile_off[g+1]*nt
-    while (hi - lo > 1) {
-        int mid = (lo + hi) >> 1;
-        if (p.tile_off[mid] * p.nt <= tile)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    while (lo < p.groups - 1 && p.tile_off[lo + 1] * p.nt <= tile) ++lo;  // skip empty groups
-    const int mt = p.tile_off[lo + 1] - p.tile_off[lo];
-    const int local = tile - p.tile_off[lo] * p.nt;
-    ti.g = lo;
-    ti.ks = 0;
-    ti.m = local % mt;
-    ti.n = local / mt;
-    ti.row0 = p.row_off[lo];
-    ti.rows = p.row_off[lo + 1] - p.row_off[lo];
-    return ti;
-}
 
 // ---------------------------------------------------------------------------
 // the kernel
@@ -280,63 +146,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             if (!mbar_wait_or_abort(&tfull[b], use & 1, err, abort_flag)) break;
             tc_fence_after();
             const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
-            const int grow = ti.m * BM + row;  // row within the group
-            const bool valid = grow < ti.rows;
-            const size_t orow = (size_t)(ti.row0 + grow);
-            if (EPI == EPI_SWIGLU) {
-#pragma unroll 1
-                for (int j0 = 0; j0 < BN / 2; j0 += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tbase + j0, g);
-                    tmem_ld16(tbase + BN / 2 + j0, u);
-                    tmem_ld_wait();
-                    if (valid) {
-                        uint32_t packed[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float h0 = silu(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                            float h1 = silu(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                            packed[i] = (uint32_t)f32_to_bf16_rn(h0) | ((uint32_t)f32_to_bf16_rn(h1) << 16);
-                        }
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out_bf16 + orow * p.ld + ti.n * (BN / 2) + j0);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    }
-                }
-            } else {
-#pragma unroll 1
-                for (int j0 = 0; j0 < BN; j0 += 16) {
-                    uint32_t v[16];
-                    tmem_ld16(tbase + j0, v);
-                    tmem_ld_wait();
-                    const int col0 = ti.n * BN + j0;
-                    if (valid && EPI == EPI_BF16) {
-                        uint32_t packed[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i)
-                            packed[i] = (uint32_t)f32_to_bf16_rn(__uint_as_float(v[2 * i])) |
-                                        ((uint32_t)f32_to_bf16_rn(__uint_as_float(v[2 * i + 1])) << 16);
-                        uint4 *dst = reinterpret_cast<uint4 *>(p.out_bf16 + orow * p.ld + col0);
-                        dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                        dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-                    } else if (valid) {
-                        float *dst = p.out_f32 + (size_t)ti.ks * p.split_stride + orow * p.ld + col0;
-                        if (EPI == EPI_LOGITS) {
-                            const bool add_bias = p.bias && ti.ks == 0;  // once, with the first part of K
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                if (col0 + i < p.n_valid)
-                                    dst[i] = __uint_as_float(v[i]) + (add_bias ? p.bias[col0 + i] : 0.f);
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; i += 4)
-                                *reinterpret_cast<float4 *>(dst + i) =
-                                    make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
-                                                __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
-                        }
-                    }
-                }
-            }
+            epilogue_tile<EPI, false>(p, ti, tbase, row);
             tc_fence_before();
             mbar_arrive(&tempty[b]);
         }
@@ -352,7 +162,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 // ---------------------------------------------------------------------------
 // host side: tensor maps and launches
 // ---------------------------------------------------------------------------
-static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     if (!fn) {
         cudaDriverEntryPointQueryResult q;
@@ -363,6 +173,20 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
             fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
     }
     return fn;
+}
+
+bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
+                  uint32_t box_rows) {
+    auto enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // 2-D bf16 tensor [rows, K] row-major; box = 64 K-elements x box_rows rows, 128-byte swizzle.
