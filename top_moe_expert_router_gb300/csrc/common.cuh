@@ -352,6 +352,28 @@ __device__ __forceinline__ float warp_sum(float v) {
 
 __device__ __forceinline__ float silu(float g) { return g / (1.0f + __expf(-g)); }
 
+// Eight E2M1 codes (one 32-bit word, the low nibble of each byte holding the
+// lower index) to four f16 pairs, exactly: byte b -> o[b] = {code 2b, code 2b+1}.
+// The word is split into its four bytes by the unpacking move, so each pair
+// costs one hardware conversion.
+__device__ __forceinline__ void e2m1x8_to_f16x2(uint32_t w, uint32_t o[4]) {
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "mov.b32 {b0, b1, b2, b3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, b1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, b3;\n\t}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+
+// Two E4M3 values (low byte first) to an f16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
+    uint32_t o;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(o) : "h"(v));
+    return o;
+}
+
 #endif  // __CUDACC__
 
 // ---------------------------------------------------------------------------

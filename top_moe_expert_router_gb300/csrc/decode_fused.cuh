@@ -36,6 +36,7 @@
 #include <cuda_runtime.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 
@@ -90,52 +91,26 @@ __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) { return _
 __device__ __forceinline__ void fp4x16(uint2 q, float2 f[8]) {
     const uint32_t words[2] = {q.x, q.y};
 #pragma unroll
-    for (int wi = 0; wi < 2; ++wi)
+    for (int wi = 0; wi < 2; ++wi) {
+        uint32_t o[4];
+        e2m1x8_to_f16x2(words[wi], o);
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            __half2_raw hr = __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((words[wi] >> (8 * b)) & 0xFFu),
-                                                       __NV_E2M1);
-            f[wi * 4 + b] = __half22float2(*reinterpret_cast<__half2 *>(&hr));
-        }
+        for (int b = 0; b < 4; ++b) f[wi * 4 + b] = __half22float2(*reinterpret_cast<const __half2 *>(&o[b]));
+    }
+}
+
+// Sixteen E2M1 codes (8 bytes) to eight f16 pairs.
+__device__ __forceinline__ void fp4x16_h2(uint2 q, __half2 h[8]) {
+    uint32_t o[8];
+    e2m1x8_to_f16x2(q.x, o);
+    e2m1x8_to_f16x2(q.y, o + 4);
+#pragma unroll
+    for (int b = 0; b < 8; ++b) h[b] = *reinterpret_cast<const __half2 *>(&o[b]);
 }
 
 __device__ __forceinline__ float e4m3f(uint8_t s) {
     __half_raw hr = __nv_cvt_fp8_to_halfraw((__nv_fp8_storage_t)s, __NV_E4M3);
     return __half2float(*reinterpret_cast<__half *>(&hr));
-}
-
-__device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
-    uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-
-// Grid barrier over all CTAs of the (cooperative) launch: arrival counter
-// `target` = (barrier index) x (grid size), plus *hold, a test hook that is 0
-// in normal operation (nonzero: an arrival that never comes, so the bounded
-// wait runs out). Bounded wait.
-__device__ inline bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *err, volatile int *abort_flag,
-                                    const uint32_t *hold) {
-    __syncthreads();
-    __shared__ int ok;
-    if (threadIdx.x == 0) {
-        target += *reinterpret_cast<const volatile uint32_t *>(hold);
-        fence_acq_rel_gpu();
-        atomicAdd(ctr, 1u);
-        ok = 1;
-        unsigned long long t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(err, ERRBIT_TIMEOUT);
-                *abort_flag = 1;
-                ok = 0;
-                break;
-            }
-        }
-        fence_acq_rel_gpu();
-    }
-    __syncthreads();
-    return ok != 0;
 }
 
 // This CTA's stages: segment A = first-half gate/up row pairs, B = second-half
@@ -149,11 +124,6 @@ struct Plan {
     // flattened down unit index (u * d / kDnRows + c / kDnRows) of down stage t (t = s - nA - nB)
     __device__ __forceinline__ int dn_unit(int t) const { return t < nC ? c0 + t : offD + d0 + (t - nC); }
 };
-
-__device__ __forceinline__ void share(int total, int b, int G, int &start, int &count) {
-    start = (int)((long long)b * total / G);
-    count = (int)((long long)(b + 1) * total / G) - start;
-}
 
 __device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, int b, int G) {
     Plan p;
@@ -213,31 +183,6 @@ __device__ __forceinline__ Plan make_plan_weighted(const int32_t *cw, int U, int
     return p;
 }
 
-// Publish a warp's count of finished h rows (all lanes' h stores first).
-__device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
-    fence_acq_rel_gpu();
-    __syncwarp();
-    if ((threadIdx.x & 31) == 0 && n) atomicAdd(ctr, (uint32_t)n);
-}
-
-// Warp-wide bounded wait until *ctr >= target.
-__device__ __forceinline__ bool wait_rows(const uint32_t *ctr, uint32_t target, uint32_t *err,
-                                          volatile int *abort_flag) {
-    int ok = 1;
-    if ((threadIdx.x & 31) == 0) {
-        const unsigned long long t0 = global_ns();
-        while (ld_acquire(ctr) < target) {
-            if (*abort_flag || global_ns() - t0 > kWaitLimitNs) {
-                atomicOr(err, ERRBIT_TIMEOUT);
-                *abort_flag = 1;
-                ok = 0;
-                break;
-            }
-        }
-    }
-    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
-}
-
 // Sums of four rows' per-lane partials (one token), reduced together:
 // exchanging halves, lane group q (lanes 8q .. 8q+7) ends with row q, and its
 // first lane stores y[q] = sum * scale.
@@ -265,14 +210,6 @@ struct Seg {
     int tok[TM];
 };
 
-// Routing state in shared memory.
-struct Route {
-    int32_t *ids, *pos, *perm, *cnt, *off, *uniq, *scan;
-    float *w;
-    uint32_t *bm;
-    int *n_uniq;
-};
-
 template <int TM>
 __device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
     s.u = u;
@@ -281,32 +218,6 @@ __device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
     s.row0 = R.off[s.e];
 #pragma unroll
     for (int r = 0; r < TM; ++r) s.tok[r] = r < s.n_e ? R.perm[s.row0 + r] : 0;
-}
-
-// exclusive scan of a[0..n) (n <= 256) by one warp; returns the total
-__device__ inline int warp_scan256(const int32_t *a, int32_t *out, int n) {
-    const int lane = threadIdx.x & 31;
-    int vals[8], local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        vals[i] = idx < n ? a[idx] : 0;
-        local += vals[i];
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int run = incl - local;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        if (idx < n) out[idx] = run;
-        run += vals[i];
-    }
-    return __shfl_sync(0xFFFFFFFFu, incl, 31);
 }
 
 // One gate/up stage (the row pair i of expert seg.e in `st`) for an expert
@@ -403,16 +314,8 @@ __device__ __forceinline__ void gu_stage(const Args &a, const LayerW &lw, const 
                 const uint2 gqv = *reinterpret_cast<const uint2 *>(gq + bb * 8);
                 const uint2 uqv = *reinterpret_cast<const uint2 *>(uq + bb * 8);
                 __half2 gh[8], uh[8];
-#pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    const uint32_t gw_ = q < 4 ? gqv.x : gqv.y, uw_ = q < 4 ? uqv.x : uqv.y;
-                    __half2_raw g2 = __nv_cvt_fp4x2_to_halfraw2(
-                        (__nv_fp4x2_storage_t)((gw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                    __half2_raw u2 = __nv_cvt_fp4x2_to_halfraw2(
-                        (__nv_fp4x2_storage_t)((uw_ >> (8 * (q & 3))) & 0xFFu), __NV_E2M1);
-                    gh[q] = *reinterpret_cast<__half2 *>(&g2);
-                    uh[q] = *reinterpret_cast<__half2 *>(&u2);
-                }
+                fp4x16_h2(gqv, gh);
+                fp4x16_h2(uqv, uh);
                 const float sgb = e4m3f(gs[bb]), sub = e4m3f(us[bb]);
 #pragma unroll
                 for (int r = 0; r < NE; ++r) {
@@ -833,101 +736,9 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     }
 
     // ---- 2. routing, computed by every CTA in shared memory ----
-    for (int t = warp; t < T; t += kConsumers + 1)
-        topk_warp(a.ws.logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k, true);
-    if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
-    if (warp == 0 && T == 1) {
-        // one token: its k distinct experts, ascending, are the k rows
-        __syncwarp();
-        const int my = lane < k ? R.ids[lane] : 0x7FFFFFFF;
-        int rank = 0;
-        int cnt_i[8], off_i[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) cnt_i[i] = off_i[i] = 0;
-        for (int q = 0; q < k; ++q) {
-            const int o = __shfl_sync(0xFFFFFFFFu, my, q);
-            rank += o < my;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                cnt_i[i] += o == e;
-                off_i[i] += o < e;
-            }
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) {
-                R.cnt[e] = cnt_i[i];
-                R.off[e] = off_i[i];
-            }
-        }
-        if (lane < k) {
-            R.uniq[rank] = my;
-            R.perm[rank] = 0;
-            R.pos[lane] = rank;
-        }
-        if (lane == 0) {
-            R.off[E] = k;
-            *R.n_uniq = k;
-        }
-    } else if (warp == 0) {
-        // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
-        // tokens ascending within an expert
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) R.bm[e] = 0u;
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
-            if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
-        }
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) {
-            const int c = __popc(R.bm[e]);
-            R.cnt[e] = c;
-            R.scan[e] = c > 0;
-        }
-        __syncwarp();
-        const int total = warp_scan256(R.cnt, R.off, E);
-        __syncwarp();
-        const int nu = warp_scan256(R.scan, R.scan, E);
-        __syncwarp();
-        for (int e = lane; e < E; e += 32)
-            if (R.cnt[e] > 0) R.uniq[R.scan[e]] = e;
-        if (lane == 0) {
-            R.off[E] = total;
-            *R.n_uniq = nu;
-        }
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
-            const int t = p / k;
-            const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
-            R.perm[row] = t;
-            R.pos[p] = row;
-        }
-    }
-    __syncthreads();
+    route_tokens(R, a.ws.logits, T, k, E, kConsumers + 1);
     const int n_uniq = *R.n_uniq;
-    if (b == 0) {  // publish the routing records
-        for (int p = tid; p < T * k; p += kThreads) {
-            a.ws.ids[p] = R.ids[p];
-            a.ws.w[p] = R.w[p];
-            a.ws.pos[p] = R.pos[p];
-            a.ws.perm[p] = R.perm[p];
-        }
-        for (int e = tid; e < E; e += kThreads) {
-            a.ws.counts[e] = R.cnt[e];
-            a.ws.offsets[e] = R.off[e];
-            a.ws.tile_off[e] = 0;
-        }
-        for (int u = tid; u < n_uniq; u += kThreads) a.ws.uniq[u] = R.uniq[u];
-        if (tid == 0) {
-            a.ws.offsets[E] = R.off[E];
-            a.ws.tile_off[E] = 0;
-            ctrl->n_uniq = n_uniq;
-        }
-    }
+    if (b == 0) publish_records(R, a.ws, T, k, E, n_uniq, kThreads);
 
     // ---- 3./4. the weight stream ----
     // The active experts are split in two halves, H1 = the first ceil(U/2).
@@ -1183,13 +994,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                         for (int q = 0; q < kDnRows; ++q) {
                             const uint2 cq = *reinterpret_cast<const uint2 *>(qb + q * (I / 2) + bb * 8);
                             __half2 wh[8];
-#pragma unroll
-                            for (int m = 0; m < 8; ++m) {
-                                const uint32_t word = m < 4 ? cq.x : cq.y;
-                                __half2_raw r2 = __nv_cvt_fp4x2_to_halfraw2(
-                                    (__nv_fp4x2_storage_t)((word >> (8 * (m & 3))) & 0xFFu), __NV_E2M1);
-                                wh[m] = *reinterpret_cast<__half2 *>(&r2);
-                            }
+                            fp4x16_h2(cq, wh);
                             __half2 p0 = __hmul2(wh[0], hh[0]), p1 = __hmul2(wh[1], hh[1]);
 #pragma unroll
                             for (int m = 2; m < 8; m += 2) {

@@ -14,7 +14,7 @@
 //     the B tile's packed E2M1 codes (256 rows x 32 bytes) and the E4M3 block
 //     scales of its rows (16 bytes per row: the scales of 4 k-blocks, of which
 //     this k-block uses 4) into one slot of a 5-deep ring;
-//   * four converter warps widen the codes: e2m1 pair -> f16 pair (hardware
+//   * eight converter warps widen the codes: e2m1 pair -> f16 pair (hardware
 //     conversion), times the block scale in f16 (exact: the product of an
 //     e2m1 and an e4m3 value has at most 6 significant bits and lies in f16's
 //     normal range), optionally -> bf16 (exact likewise), and write the
@@ -28,7 +28,7 @@
 // 2^-p >= 1/max|x_t| (exact), the accumulator multiplied back by 2^p and the
 // tensor scale; down: A = h in bf16, B widened to bf16.
 // Warp roles: 0 = TMA producer, 1 = MMA issuer (owns TMEM), 2..5 = epilogue,
-// 6..9 = converters.
+// 6..13 = converters.
 #include <cuda_fp16.h>
 #include <cuda_fp4.h>
 #include <cuda_fp8.h>
@@ -41,9 +41,9 @@ namespace fp4gemm {
 
 constexpr int kQStages = 5;                       // TMA ring depth
 constexpr int kBStages = 2;                       // converted-tile buffers
-constexpr int kConvWarps = 4;
+constexpr int kConvWarps = 8;                     // two per SM sub-partition: conversion latency hidden
 constexpr int kConvThreads = 32 * kConvWarps;
-constexpr int kThreads = 192 + kConvThreads;      // producer, MMA, 4 epilogue, 4 converter warps
+constexpr int kThreads = 192 + kConvThreads;      // producer, MMA, 4 epilogue, 8 converter warps
 constexpr uint32_t kABytes = BM * BK * 2;         // 16 KB
 constexpr uint32_t kCodeBytes = BN * BK / 2;      // 8 KB: 256 rows x 32 B
 constexpr uint32_t kScaleRowBytes = 16;           // the scales of 4 k-blocks
@@ -59,20 +59,18 @@ template <bool BF16OUT>
 __device__ __forceinline__ void convert_item(const unsigned char *codes, const unsigned char *scales,
                                              unsigned char *btile, int row, int half) {
     const uint4 cw = *reinterpret_cast<const uint4 *>(codes);
-    const uint16_t sc2 = *reinterpret_cast<const uint16_t *>(scales);
-    const __half2_raw sr = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)sc2, __NV_E4M3);
-    const __half2 s = *reinterpret_cast<const __half2 *>(&sr);
+    const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(scales));
+    const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
     const __half2 s_lo = __low2half2(s), s_hi = __high2half2(s);   // blocks 2*half, 2*half + 1
     const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
         const __half2 sj = j < 2 ? s_lo : s_hi;
         uint32_t o[4];
+        e2m1x8_to_f16x2(words[j], o);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const __half2_raw hr =
-                __nv_cvt_fp4x2_to_halfraw2((__nv_fp4x2_storage_t)((words[j] >> (8 * b)) & 0xFFu), __NV_E2M1);
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&hr), sj);
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[b]), sj);
             if (BF16OUT) {
                 const __nv_bfloat162 bv = __float22bfloat162_rn(__half22float2(v));
                 o[b] = *reinterpret_cast<const uint32_t *>(&bv);
@@ -223,7 +221,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------- converters --------------------------------
-        const int ct = threadIdx.x - 192;   // 0 .. 127
+        const int ct = threadIdx.x - 192;   // 0 .. kConvThreads - 1
         int it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
@@ -238,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const unsigned char *scales = codes + kCodeBytes + (kb & 3) * 4;
                 unsigned char *bt = btiles + (size_t)bs * kBBytes;
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
+                for (int i = 0; i < 2 * BN / kConvThreads; ++i) {   // 512 items: (row, half) of 256 rows
                     const int item = ct + kConvThreads * i;
                     const int row = item >> 1, half = item & 1;
                     convert_item<!F16>(codes + row * (BK / 2) + half * 16, scales + row * kScaleRowBytes + half * 2,
