@@ -133,6 +133,22 @@ moe_status moe_forward_host(moe_layer *layer, const void *x_host, void *out_host
  * output precision) and are widened to fp32 here. */
 moe_status moe_debug_expert_outputs(moe_layer *layer, float *Y, int T, void *stream);
 
+/* Small-batch (T <= 16) kernel choice. Both compute the same layer in one
+ * persistent launch; they differ in where the expert FFNs run:
+ *   MOE_DECODE_CUDA_CORES: each weight row is multiplied by the tokens on the
+ *     CUDA cores as it streams in (suits one token with bf16 weights, where
+ *     the stream alone sets the pace);
+ *   MOE_DECODE_TENSOR_CORES: 128 weight rows at a time are the M operand of
+ *     tcgen05.mma and the tokens the N = 16 operand, NVFP4 codes widened into
+ *     tensor memory on the way (suits several tokens or NVFP4 weights);
+ *   MOE_DECODE_AUTO (default): the tensor cores for NVFP4 experts and for 4 or
+ *     more tokens, else the CUDA cores.
+ * The tensor-core kernel needs d % 128 == 0 and no expert_out_norm; where a
+ * layer does not meet that, the CUDA-core kernel runs whatever the choice.
+ * Stacks follow the choice of their first layer. */
+enum { MOE_DECODE_AUTO = 0, MOE_DECODE_CUDA_CORES = 1, MOE_DECODE_TENSOR_CORES = 2 };
+moe_status moe_set_decode_path(moe_layer *layer, int path);
+
 /* Routing records of the last forward or route on this layer, as the
  * kernels left them in the workspace (no recomputation): the fields of
  * moe_route, same layouts; any output pointer may be NULL. A forward of
@@ -189,7 +205,8 @@ moe_status moe_profile_end(moe_layer *layer, float *ms_host, int max_kernels, in
  * owns all device memory and hands it only input and output buffers, or a
  * real-time loop that forbids allocation after start-up).
  *
- * Same result as moe_forward for 1 <= T <= 16 tokens, with no layer object
+ * Same result as moe_forward on the CUDA-core small-batch kernel
+ * (MOE_DECODE_CUDA_CORES) for 1 <= T <= 16 tokens, with no layer object
  * and no workspace: the scratch lives in one static device array of
  * MOE_STATIC_SCRATCH_BYTES that every GPU which loads libmoe.so holds until
  * the process exits. The call allocates nothing (no cudaMalloc, no

@@ -54,10 +54,12 @@ def _quantize_on_gpu(moe, g, u, d):
     return packs
 
 
-@pytest.mark.parametrize("T", [1, 4, 16, 17, 40, 300])
-def test_small_nvfp4_layer(gpu_lib, T):
-    """T <= 16: the single-launch decode kernel; T > 16: the NVFP4 grouped
-    GEMMs (several 128-row tiles per expert and ragged tails at T = 300)."""
+@pytest.mark.parametrize("T,path", [(1, 1), (4, 1), (16, 1), (1, 2), (4, 2), (16, 2), (17, 0), (40, 0), (300, 0)])
+def test_small_nvfp4_layer(gpu_lib, T, path):
+    """T <= 16: the single-launch decode kernels (path 1: CUDA cores, 2:
+    tensor cores with the codes widened into tensor memory); T > 16: the
+    NVFP4 grouped GEMMs (several 128-row tiles per expert and ragged tails at
+    T = 300)."""
     w = datagen.Workload("fp4small", T=T, d=512, E=64, k=8, I=256, fmt="nvfp4", router_scale=4.0)
     wr = datagen.router_weights(w)
     g, u, d = datagen.expert_weights(w)
@@ -70,6 +72,7 @@ def test_small_nvfp4_layer(gpu_lib, T):
         np.testing.assert_array_equal(packs["g_" + name].cpu().numpy(), gs)
         host["q_" + name], host["s_" + name], host["g_" + name] = q, s, gs
     gl = _nvfp4_gpu_layer(gpu_lib, wr, None, packs, w.k, 512)
+    gl.set_decode_path(path)
     L = oracle.Layer(wr, k=w.k, nvfp4=host)
     x = datagen.tokens(w, T, start_row=3)
     xd = to_dev_bf16(x)

@@ -96,6 +96,22 @@ def test_tiny_every_token(tiny, T):
     assert st["err"] < 5e-3
 
 
+@pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
+@pytest.mark.parametrize("T", [1, 2, 5, 16])
+def test_tiny_both_decode_kernels(gpu_lib, T, path):
+    """The two single-launch small-batch kernels (experts on CUDA cores, or
+    on the tensor cores with the tokens as the N = 16 operand), each against
+    the oracle on every token and every expert slot."""
+    host = HostLayer(W["tiny"])
+    gl = _gpu_layer(gpu_lib, host, max_tokens=16)
+    gl.set_decode_path(gpu_lib.MOE_DECODE_CUDA_CORES if path == "cuda_cores" else gpu_lib.MOE_DECODE_TENSOR_CORES)
+    x = datagen.tokens(host.w, T, start_row=700 + T)
+    st = _parity(gl, host.oracle(), x, host.w.E, BF16_TOL)
+    assert gl.last_launch_count() == 1
+    assert st["err"] < 5e-3
+    gl.close()
+
+
 def test_chunked_path_for_shapes_the_gemms_do_not_take(gpu_lib):
     """A bf16 layer whose hidden size is not a multiple of 256 (d = 320) runs
     batches above 16 tokens in chunks of 16 through the split streaming
@@ -108,6 +124,26 @@ def test_chunked_path_for_shapes_the_gemms_do_not_take(gpu_lib):
     st = _parity(gl, host.oracle(), x, w.E, BF16_TOL, check_Y=False, check_records=False)
     assert gl.last_launch_count() == 3 * 4          # three chunks of four launches
     assert st["err"] < 5e-3
+
+
+@pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
+def test_alternating_inputs_read_nothing_stale(gpu_lib, path):
+    """Successive forwards on one layer with different tokens: every result
+    matches the oracle. The workspace then always holds the previous call's
+    token rows, h and expert outputs, so a hand-off that read them before the
+    current call rewrote them (a missing wait) shows up as a wrong token."""
+    host = HostLayer(W["tiny"])
+    gl = _gpu_layer(gpu_lib, host, max_tokens=16)
+    gl.set_decode_path(gpu_lib.MOE_DECODE_CUDA_CORES if path == "cuda_cores" else gpu_lib.MOE_DECODE_TENSOR_CORES)
+    L = host.oracle()
+    for i, T in enumerate([16, 16, 5, 16, 3, 16, 9, 16]):
+        x = datagen.tokens(host.w, T, start_row=3000 + 41 * i)
+        y = gl.forward(to_dev_bf16(x))
+        torch.cuda.synchronize()
+        err = normwise_rel_err(datagen.bf16_to_f32(bf16_host(y)), L.forward(x)["y"])
+        assert err.max() < 1e-2, f"call {i} (T={T}): {err.max():.3g}"
+    assert gl.device_status() == 0
+    gl.close()
 
 
 def test_tiny_route_large_batch(tiny):
@@ -190,10 +226,13 @@ def test_rmsnorm_matches_oracle(gpu_lib):
 # full-size layer d=4096, E=256, I=1536
 # --------------------------------------------------------------------------
 
+@pytest.mark.parametrize("path", ["auto", "cuda_cores", "tensor_cores"])
 @pytest.mark.parametrize("T,start", [(4, 100), (16, 200)])
-def test_decode_full_size_every_token(gpu_lib, full_layer, T, start):
+def test_decode_full_size_every_token(gpu_lib, full_layer, T, start, path):
     host, dev = full_layer
     gl = _full_gpu_layer(gpu_lib, dev, max_tokens=16, bias=False)
+    gl.set_decode_path({"auto": gpu_lib.MOE_DECODE_AUTO, "cuda_cores": gpu_lib.MOE_DECODE_CUDA_CORES,
+                        "tensor_cores": gpu_lib.MOE_DECODE_TENSOR_CORES}[path])
     x = datagen.tokens(D4096, T, start_row=start)
     st = _parity(gl, host.oracle(bias=False), x, 256, BF16_TOL)
     assert st["err"] < 1e-2

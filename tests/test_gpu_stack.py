@@ -35,10 +35,15 @@ def _bf16_layers(moe, w, n):
     return layers, host
 
 
+@pytest.mark.parametrize("path", [1, 2])
 @pytest.mark.parametrize("T", [1, 3, 8])
-def test_stack_bf16_matches_layer_by_layer(gpu_lib, T):
+def test_stack_bf16_matches_layer_by_layer(gpu_lib, T, path):
+    """path 1: the CUDA-core kernel, 2: the tensor-core kernel, for the stack
+    and for the layer-by-layer reference alike."""
     w = datagen.WORKLOADS["tiny"]
     layers, host = _bf16_layers(gpu_lib, w, 3)
+    for gl in layers:
+        gl.set_decode_path(path)
     x = to_dev_bf16(datagen.tokens(w, T, start_row=40))
     stack = gpu_lib.MoeStack(layers)
     lo = torch.empty((3, T, w.d), dtype=torch.bfloat16, device="cuda")
@@ -62,8 +67,10 @@ def test_stack_bf16_matches_layer_by_layer(gpu_lib, T):
     assert (np.abs(got - want) <= bound).all()
 
 
-def test_stack_nvfp4_matches_layer_by_layer(gpu_lib):
-    """4 NVFP4 layers of the full width (d=4096, I=1536), 32 experts each, T=4."""
+@pytest.mark.parametrize("path", [1, 2])
+def test_stack_nvfp4_matches_layer_by_layer(gpu_lib, path):
+    """4 NVFP4 layers of the full width (d=4096, I=1536), 32 experts each, T=4
+    (path 1: CUDA-core kernel, 2: tensor-core kernel)."""
     w = datagen.Workload("fp4stack", T=4, d=4096, E=32, k=8, I=1536, fmt="nvfp4",
                          router_scale=datagen.ROUTER_SCALE_D4096)
     layers = []
@@ -75,6 +82,7 @@ def test_stack_nvfp4_matches_layer_by_layer(gpu_lib):
             q, s, gs = gpu_lib.quantize_nvfp4(to_dev_bf16(arr))
             packs["q_" + name], packs["s_" + name], packs["g_" + name] = q, s, gs
         layers.append(gpu_lib.MoeLayer(to_dev_bf16(wr), nvfp4=packs, top_k=8, max_tokens=16))
+        layers[-1].set_decode_path(path)
     x = to_dev_bf16(datagen.tokens(w, 4, start_row=8))
     stack = gpu_lib.MoeStack(layers)
     lo = torch.empty((4, 4, w.d), dtype=torch.bfloat16, device="cuda")

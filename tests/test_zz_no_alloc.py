@@ -35,6 +35,8 @@ def test_static_scratch_forward_matches_forward(gpu_lib, shape):
     else:   # full hidden and expert widths, fewer experts to keep the layer small
         w = datagen.Workload("d4096_e16", T=16, d=4096, E=16, k=8, I=1536, router_scale=datagen.ROUTER_SCALE_D4096)
     layer = _layer(gpu_lib, w)
+    # the no-alloc call runs the CUDA-core small-batch kernel: compare with the same kernel
+    layer.set_decode_path(gpu_lib.MOE_DECODE_CUDA_CORES)
     lib = gpu_lib.load()
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     # the call ignores max_tokens: the second call passes a copy with 0 there

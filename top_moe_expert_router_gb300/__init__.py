@@ -23,6 +23,7 @@ HEADER = os.path.join(_build.ROOT, "include", "moe.h")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_DEVICE, MOE_ERR_TIMEOUT = range(6)
 MOE_W_BF16, MOE_W_NVFP4 = 0, 1
+MOE_DECODE_AUTO, MOE_DECODE_CUDA_CORES, MOE_DECODE_TENSOR_CORES = 0, 1, 2
 
 
 class MoeError(RuntimeError):
@@ -75,6 +76,7 @@ def load(path: str | None = None):
             "moe_debug_expert_outputs": ([vp, vp, i, vp], st),
             "moe_debug_route_records": ([vp, i, vp, vp, vp, vp, vp, vp, vp], st),
             "moe_debug_hold_grid_barrier": ([vp, i, vp], st),
+            "moe_set_decode_path": ([vp, i], st),
             "moe_rmsnorm": ([vp, vp, i, i, f, vp], st),
             "moe_quantize_nvfp4": ([vp, i, i, i, vp, vp, vp, vp], st),
             "moe_get_device_status": ([vp, vp], st),
@@ -194,6 +196,10 @@ class MoeLayer:
         _check(load().moe_debug_route_records(self._h, T, *(_ptr(out[n]) for n in self._RECORDS),
                                               _stream(stream)), "moe_debug_route_records")
         return out
+
+    def set_decode_path(self, path: int):
+        """MOE_DECODE_AUTO, MOE_DECODE_CUDA_CORES or MOE_DECODE_TENSOR_CORES (T <= 16)."""
+        _check(load().moe_set_decode_path(self._h, int(path)), "moe_set_decode_path")
 
     def hold_grid_barrier(self, hold: bool, stream=None):
         """Test hook: make the decode kernel's grid barriers wait for an arrival

@@ -14,6 +14,9 @@ struct moe_layer {
     moe::LayerDev L;
     moe::Workspace ws;
     int last_launches;
+    int decode_path = MOE_DECODE_AUTO;
+    bool mma_maps_ok = false;            // the tensor-core decode kernel's tensor maps are encoded
+    std::vector<unsigned char> mma_maps;  // host copy, passed by value at launch
     bool y_bf16 = false;  // the last forward left the expert outputs in bf16 over ws.xperm
     // profiling: events [forward][kernel boundary]
     std::vector<cudaEvent_t> prof_events;
@@ -106,6 +109,16 @@ moe_status forward_prefill(moe_layer *ly, const uint16_t *x, const uint16_t *res
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// Which small-batch kernel runs T tokens: the tensor-core layer kernel
+// (decode_mma) or the CUDA-core one (decode_fused). By default the tensor
+// cores take NVFP4 experts and batches of several tokens, where the CUDA
+// cores' arithmetic, not the weight stream, would set the pace.
+bool use_mma(const moe_layer *ly, int T) {
+    if (ly->decode_path == MOE_DECODE_CUDA_CORES || !ly->mma_maps_ok || !mma_supported(ly->L, T)) return false;
+    if (ly->decode_path == MOE_DECODE_TENSOR_CORES) return true;
+    return ly->L.fmt == MOE_W_NVFP4 || T >= 4;
+}
+
 // Forward on device buffers; res may be NULL.
 moe_status forward_impl(moe_layer *ly, const uint16_t *x, const uint16_t *res, uint16_t *out, int T,
                         cudaStream_t st) {
@@ -114,10 +127,12 @@ moe_status forward_impl(moe_layer *ly, const uint16_t *x, const uint16_t *res, u
     const int tdec = decode_max_tokens(L.d);
     if (T > tdec && prefill_supported(L)) return forward_prefill(ly, x, res, out, T, st);
     ly->y_bf16 = false;
-    if (T <= tdec) {
+    const bool mma = T <= 16 && use_mma(ly, T);
+    if (T <= tdec || mma) {
         // the whole layer in one persistent launch
         prof_mark(ly, 0, st);
-        cudaError_t e = launch_decode_fused(L, ly->ws, x, res, out, T, st);
+        cudaError_t e = mma ? launch_decode_mma(L, ly->ws, ly->mma_maps.data(), x, res, out, T, st)
+                            : launch_decode_fused(L, ly->ws, x, res, out, T, st);
         prof_mark(ly, 1, st);
         ly->last_launches = L.expert_norm ? 2 : 1;
         if (ly->prof_count < ly->prof_max) {
@@ -217,7 +232,16 @@ moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t 
     L.expert_norm = desc->expert_out_norm ? 1 : 0;
     ly->ws = ws;
     ly->last_launches = 0;
+    ly->mma_maps.assign(mma_maps_bytes(), 0);
+    const LayerW w{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+    ly->mma_maps_ok = mma_encode_maps(L, w, ws, ly->mma_maps.data());
     *out = ly;
+    return MOE_OK;
+}
+
+moe_status moe_set_decode_path(moe_layer *ly, int path) {
+    if (!ly || path < MOE_DECODE_AUTO || path > MOE_DECODE_TENSOR_CORES) return MOE_ERR_INVALID_ARG;
+    ly->decode_path = path;
     return MOE_OK;
 }
 
@@ -365,6 +389,20 @@ moe_status moe_stack_create(moe_layer *const *layers, int n_layers, moe_stack **
     if (cudaMemcpy(layers[0]->ws.stack, w.data(), sizeof(LayerW) * (size_t)n_layers, cudaMemcpyHostToDevice) !=
         cudaSuccess)
         return MOE_ERR_CUDA;
+    // the tensor-core kernel's maps of every layer (weights of layer l; token
+    // rows and h in the first layer's workspace, which the stack runs on)
+    if (layers[0]->mma_maps_ok) {
+        const size_t mb = mma_maps_bytes();
+        std::vector<unsigned char> maps(mb * (size_t)n_layers);
+        bool ok = true;
+        for (int l = 0; l < n_layers && ok; ++l) {
+            LayerDev Ll = L0;
+            ok = mma_encode_maps(Ll, w[(size_t)l], layers[0]->ws, maps.data() + mb * (size_t)l);
+        }
+        if (ok && cudaMemcpy(layers[0]->ws.tmaps, maps.data(), maps.size(), cudaMemcpyHostToDevice) != cudaSuccess)
+            return MOE_ERR_CUDA;
+        if (!ok) layers[0]->mma_maps_ok = false;
+    }
     *out = new moe_stack{layers[0], n_layers};
     return MOE_OK;
 }
@@ -375,8 +413,11 @@ moe_status moe_stack_forward(moe_stack *sk, const void *x, void *out, int T, flo
         T > 8 || T > sk->first->L.max_T || !(eps >= 0.f))
         return MOE_ERR_INVALID_ARG;
     moe_layer *ly = sk->first;
-    const cudaError_t e = launch_decode_stack(ly->L, ly->ws, sk->n_layers, eps, (const uint16_t *)x,
-                                              (uint16_t *)out, (uint16_t *)layer_out, T, (cudaStream_t)stream);
+    const cudaError_t e =
+        use_mma(ly, T) ? launch_decode_mma_stack(ly->L, ly->ws, sk->n_layers, eps, (const uint16_t *)x, (uint16_t *)out,
+                                                 (uint16_t *)layer_out, T, (cudaStream_t)stream)
+                       : launch_decode_stack(ly->L, ly->ws, sk->n_layers, eps, (const uint16_t *)x, (uint16_t *)out,
+                                             (uint16_t *)layer_out, T, (cudaStream_t)stream);
     ly->last_launches = 1;
     if (e == cudaErrorInvalidValue || e == cudaErrorInvalidConfiguration) return MOE_ERR_UNSUPPORTED;
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;

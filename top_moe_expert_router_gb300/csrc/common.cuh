@@ -87,6 +87,9 @@ struct Workspace {
     float *Y;           // [max_T*k, d] fp32 expert outputs
     uint16_t *xperm;    // [max_T*k, d] bf16 gathered rows (prefill; f16 for NVFP4 experts)
     float *row_scale;   // [max_T*k] NVFP4 prefill: power-of-two scale of each gathered row
+    uint16_t *xb;       // [16, d] tensor-core decode: the token rows of the B operand (bf16 / scaled f16)
+    float *xscale;      // [16] tensor-core decode, NVFP4: per-token power-of-two scales
+    void *tmaps;        // [kMaxStack] tensor-core decode: each stacked layer's tensor maps (1 KB each)
     int32_t *chunk_base;  // [ceil(max_T/kRouteChunk), E] per-chunk counts, then each chunk's first row per expert
     uint32_t *chunk_bm;   // [ceil(max_T/kRouteChunk), E] token bitmaps of each kRouteChunk-token chunk
     size_t bytes;
@@ -135,6 +138,9 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     ws.Y = (float *)take(sizeof(float) * Tk * d);
     ws.xperm = (uint16_t *)take(sizeof(uint16_t) * Tk * d);
     ws.row_scale = (float *)take(sizeof(float) * Tk);
+    ws.xb = (uint16_t *)take(sizeof(uint16_t) * 16 * (size_t)d);
+    ws.xscale = (float *)take(sizeof(float) * 16);
+    ws.tmaps = take((size_t)1024 * kMaxStack);
     const size_t nchunks = ((size_t)max_T + kRouteChunk - 1) / kRouteChunk;
     ws.chunk_base = (int32_t *)take(sizeof(int32_t) * nchunks * E);
     ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E);
@@ -417,6 +423,17 @@ cudaError_t launch_gather_rows(const LayerDev &L, const Workspace &ws, const uin
 cudaError_t launch_router_gemm(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
 cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st,
                                    int *launches);
+// decode_mma.cu: the tensor-core small-batch layer (T <= 16). The tensor maps
+// of a layer (weights, token rows, h) are encoded once on the host into a
+// 1 KB block; mma_maps_bytes() gives its size.
+size_t mma_maps_bytes();
+bool mma_encode_maps(const LayerDev &L, const LayerW &w, const Workspace &ws, void *maps_host);
+bool mma_supported(const LayerDev &L, int T);
+cudaError_t launch_decode_mma(const LayerDev &L, const Workspace &ws, const void *maps_host, const uint16_t *x,
+                              const uint16_t *res, uint16_t *out, int T, cudaStream_t st);
+// n_layers stacked layers, their maps in ws.tmaps (copied there by the caller)
+cudaError_t launch_decode_mma_stack(const LayerDev &L, const Workspace &ws, int n_layers, float eps,
+                                    const uint16_t *x, uint16_t *out, uint16_t *layer_out, int T, cudaStream_t st);
 // prefill_fp4.cu
 cudaError_t launch_gather_rows_f16(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st);
 cudaError_t launch_prefill_experts_fp4(const LayerDev &L, const Workspace &ws, int T, cudaStream_t st,

@@ -50,6 +50,30 @@ __device__ __forceinline__ void share(int total, int b, int G, int &start, int &
     count = (int)((long long)(b + 1) * total / G) - start;
 }
 
+// This CTA's stages: segment A = first-half gate/up row pairs, B = second-half
+// gate/up, C = first-half down units (kDnRows rows), D = second-half down.
+struct Plan {
+    int nA, nB, nC, nD;        // stages of each segment in this CTA
+    int a0, b0, c0, d0;        // first index of this CTA's share within each segment
+    int offB, offD;            // global start of the second-half segments
+    // flattened gate/up row-pair index (u * I + i) of gate/up stage s
+    __device__ __forceinline__ int gu_row(int s) const { return s < nA ? a0 + s : offB + b0 + (s - nA); }
+    // flattened down unit index (u * d / kDnRows + c / kDnRows) of down stage t (t = s - nA - nB)
+    __device__ __forceinline__ int dn_unit(int t) const { return t < nC ? c0 + t : offD + d0 + (t - nC); }
+};
+
+__device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, int b, int G) {
+    Plan p;
+    const int U1 = (U + 1) / 2, U2 = U - U1;
+    share(U1 * I, b, G, p.a0, p.nA);
+    share(U2 * I, b, G, p.b0, p.nB);
+    share(U1 * units_per_expert, b, G, p.c0, p.nC);
+    share(U2 * units_per_expert, b, G, p.d0, p.nD);
+    p.offB = U1 * I;
+    p.offD = U1 * units_per_expert;
+    return p;
+}
+
 // Publish a warp's count of finished h rows (all lanes' h stores first).
 __device__ __forceinline__ void publish_rows(uint32_t *ctr, int n) {
     fence_acq_rel_gpu();
