@@ -198,8 +198,10 @@ def test_residual_forward(tiny):
     ref = host.oracle().forward(x)
     want = datagen.bf16_to_f32(oracle.residual_add(res, ref["y"]))
     got = datagen.bf16_to_f32(bf16_host(out))
-    # within one bf16 rounding of the sum plus the layer tolerance on the MoE part
-    bound = np.abs(want) * 2 ** -8 + BF16_TOL * np.abs(ref["y"]).max(1, keepdims=True)
+    # within one bf16 spacing of the sum (the MoE part, within its tolerance, may
+    # move the sum across a rounding boundary; a spacing is at most 2^-7 of the
+    # value) plus the layer tolerance on the MoE part
+    bound = np.abs(want) * 2 ** -7 + BF16_TOL * np.abs(ref["y"]).max(1, keepdims=True)
     assert (np.abs(got - want) <= bound).all()
 
 
