@@ -47,6 +47,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 FLUSH_BYTES = 256 << 20
 POOL = 64
 HEADLINE = "decode_t1"
+DECODE_PATHS = {"auto": 0, "cuda_cores": 1, "tensor_cores": 2}
 ORDER = ["decode_t1", "decode_t4", "decode_t16", "prefill_t4096", "nvfp4_prefill_t4096", "nvfp4_stack_t4"]
 
 
@@ -60,9 +61,13 @@ def parse_args(argv=None):
     p.add_argument("--steps", type=int, default=200)
     p.add_argument("--warmup", type=int, default=10)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    p.add_argument("--workload", default="all", choices=["all"] + ORDER)
+    p.add_argument("--workload", default="all", choices=["all"] + sorted(datagen.WORKLOADS))
+    p.add_argument("--gate-up-layout", choices=["separate", "interleaved"], default="separate",
+                   help="bf16 gate/up weights as two [E, I, d] tensors, or one [E, I, 2, d] interleaved by row")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--e2e-steps", type=int, default=200)
+    p.add_argument("--decode-path", choices=["auto", "cuda_cores", "tensor_cores"], default="auto",
+                   help="small-batch kernel (T <= 16): the library's choice, or one forced")
     p.add_argument("--experts", type=int, default=0,
                    help="override E (a smaller layer of the same kernels, for profiler captures)")
     return p.parse_args(argv)
@@ -563,6 +568,7 @@ def build_stack(ctx, w):
         torch.cuda.synchronize()
         torch.cuda.empty_cache()
         layers.append(moe.MoeLayer(ctx.bf(wr), nvfp4=packs, top_k=w.k, max_tokens=max(w.T, 16)))
+        layers[-1].set_decode_path(DECODE_PATHS[ctx.args.decode_path])
     return layers
 
 
@@ -630,6 +636,7 @@ def run_ours(args):
     moe.load()
     ctx = Ctx(args, moe, device, dist, rank, world, local_rank)
     names = ORDER if args.workload == "all" else [args.workload]
+    extra_cfg = {"gate_up_layout": args.gate_up_layout, "decode_path": args.decode_path}
     results = {}
 
     bf16_names = [n for n in names if datagen.WORKLOADS[n].fmt == "bf16"]
@@ -644,14 +651,21 @@ def run_ours(args):
         g, u, d = datagen.expert_weights(w0)
         dev = {"wr": ctx.bf(wr), "gate": ctx.bf(g), "up": ctx.bf(u), "down": ctx.bf(d)}
         del g, u, d
+        if args.gate_up_layout == "interleaved":
+            dev["gate_up"] = torch.stack((dev["gate"], dev["up"]), dim=2).contiguous()   # [E, I, 2, d]
         for n in bf16_names:
             w = datagen.WORKLOADS[n]
             if args.experts:
                 w = dataclasses.replace(w, E=args.experts)
             bias = datagen.router_bias(w)
-            gl = moe.MoeLayer(dev["wr"], w_gate=dev["gate"], w_up=dev["up"], w_down=dev["down"],
-                              router_bias=None if bias is None else torch.from_numpy(bias).to(device),
-                              top_k=w.k, max_tokens=max(w.T, 16))
+            wb = None if bias is None else torch.from_numpy(bias).to(device)
+            if args.gate_up_layout == "interleaved":
+                gl = moe.MoeLayer(dev["wr"], w_gate_up=dev["gate_up"], w_down=dev["down"], router_bias=wb,
+                                  top_k=w.k, max_tokens=max(w.T, 16))
+            else:
+                gl = moe.MoeLayer(dev["wr"], w_gate=dev["gate"], w_up=dev["up"], w_down=dev["down"], router_bias=wb,
+                                  top_k=w.k, max_tokens=max(w.T, 16))
+            gl.set_decode_path(DECODE_PATHS[args.decode_path])
             fn = measure_prefill if w.T > 16 else measure_decode
             results[n] = fn(ctx, w, gl, (wr, bias))
             gl.close()
@@ -692,7 +706,7 @@ def run_ours(args):
             "metric": METRIC, "value": head["value"], "unit": "tok/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": head.get("dtype", "bf16"), "data": "synthetic",
-            "config": dict(head["config"], parallelism=f"replicas x{world}, tokens split by rank"),
+            "config": dict(head["config"], parallelism=f"replicas x{world}, tokens split by rank", **extra_cfg),
             "roofline": head["roofline"],
             "cpu_baseline": head.get("cpu_baseline"),
             "e2e": head["e2e"],

@@ -155,6 +155,8 @@ WORKLOADS = {
                           router_scale=ROUTER_SCALE_D4096),
     "decode_t4": Workload("decode_t4", T=4, d=4096, E=256, k=8, I=1536,
                           router_scale=ROUTER_SCALE_D4096),
+    "decode_t8": Workload("decode_t8", T=8, d=4096, E=256, k=8, I=1536,
+                          router_scale=ROUTER_SCALE_D4096),
     "decode_t16": Workload("decode_t16", T=16, d=4096, E=256, k=8, I=1536,
                            router_scale=ROUTER_SCALE_D4096),
     "prefill_t4096": Workload("prefill_t4096", T=4096, d=4096, E=256, k=8, I=1536,

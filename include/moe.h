@@ -89,6 +89,12 @@ typedef struct {
      * a reading of "Muse Spark normalises each expert's output, then combines"
      * ("TensorSharp Muse Spark benchmark", section "Performance"). */
     int expert_out_norm;
+    /* bf16 experts only. 0: w_gate and w_up are separate [E, I, d] tensors.
+     * 1: w_gate points to one [E, I, 2, d] tensor holding gate row i then up
+     * row i of each expert (the fused gate/up projection, interleaved by row)
+     * and w_up is ignored; the small-batch kernels then fetch a row pair as one
+     * contiguous copy. */
+    int gate_up_interleaved;
 } moe_layer_desc;
 
 /* Bytes of device workspace the layer needs (for max_tokens). No GPU work. */
@@ -141,7 +147,7 @@ moe_status moe_debug_expert_outputs(moe_layer *layer, float *Y, int T, void *str
  *   MOE_DECODE_TENSOR_CORES: 128 weight rows at a time are the M operand of
  *     tcgen05.mma and the tokens the N = 16 operand, NVFP4 codes widened into
  *     tensor memory on the way (suits several tokens or NVFP4 weights);
- *   MOE_DECODE_AUTO (default): the tensor cores for NVFP4 experts and for 4 or
+ *   MOE_DECODE_AUTO (default): the tensor cores for bf16 experts and 8 or
  *     more tokens, else the CUDA cores.
  * The tensor-core kernel needs d % 128 == 0 and no expert_out_norm; where a
  * layer does not meet that, the CUDA-core kernel runs whatever the choice.

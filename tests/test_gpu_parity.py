@@ -146,6 +146,23 @@ def test_alternating_inputs_read_nothing_stale(gpu_lib, path):
     gl.close()
 
 
+@pytest.mark.parametrize("T,path", [(1, 1), (5, 1), (16, 1), (5, 2), (16, 2), (40, 0)])
+def test_interleaved_gate_up_layout(gpu_lib, T, path):
+    """gate/up weights as one [E, I, 2, d] tensor interleaved by row (gate row
+    i, then up row i): the small-batch kernels (path 1: CUDA cores, 2: tensor
+    cores) and the prefill GEMMs (T = 40) against the oracle, which keeps the
+    two matrices separate."""
+    host = HostLayer(W["tiny"])
+    gu = np.ascontiguousarray(np.stack([host.gate, host.up], axis=2))      # [E, I, 2, d]
+    gl = gpu_lib.MoeLayer(to_dev_bf16(host.wr), w_gate_up=to_dev_bf16(gu), w_down=to_dev_bf16(host.down),
+                          top_k=host.w.k, max_tokens=64)
+    gl.set_decode_path(path)
+    x = datagen.tokens(host.w, T, start_row=4000 + T)
+    st = _parity(gl, host.oracle(), x, host.w.E, BF16_TOL)
+    assert st["err"] < 5e-3
+    gl.close()
+
+
 def test_tiny_route_large_batch(tiny):
     """The multi-kernel routing path (T > 32): router GEMM, top-k, permutation."""
     host, gl = tiny

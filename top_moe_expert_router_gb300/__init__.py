@@ -42,6 +42,7 @@ class MoeLayerDesc(ctypes.Structure):
         ("s_gate", ctypes.c_void_p), ("s_up", ctypes.c_void_p), ("s_down", ctypes.c_void_p),
         ("g_gate", ctypes.c_void_p), ("g_up", ctypes.c_void_p), ("g_down", ctypes.c_void_p),
         ("expert_out_norm", ctypes.c_int),
+        ("gate_up_interleaved", ctypes.c_int),
     ]
 
 
@@ -133,7 +134,7 @@ class MoeLayer:
     The workspace is allocated here with torch; the library allocates nothing.
     """
 
-    def __init__(self, w_router, *, w_gate=None, w_up=None, w_down=None, nvfp4=None,
+    def __init__(self, w_router, *, w_gate=None, w_up=None, w_down=None, nvfp4=None, w_gate_up=None,
                  router_bias=None, top_k=8, max_tokens=16, expert_out_norm=False):
         lib = load()
         E, d = w_router.shape
@@ -144,7 +145,15 @@ class MoeLayer:
         self._keep = [w_router, router_bias]
         desc.w_router = _ptr(w_router)
         desc.router_bias = _ptr(router_bias)
-        if nvfp4 is None:
+        if w_gate_up is not None:
+            # [E, I, 2, d]: gate row i then up row i of each expert
+            _require_cuda(w_router, w_gate_up, w_down, router_bias)
+            self.I = w_gate_up.shape[1]
+            desc.fmt = MOE_W_BF16
+            desc.gate_up_interleaved = 1
+            desc.w_gate, desc.w_up, desc.w_down = _ptr(w_gate_up), None, _ptr(w_down)
+            self._keep += [w_gate_up, w_down]
+        elif nvfp4 is None:
             _require_cuda(w_router, w_gate, w_up, w_down, router_bias)
             self.I = w_gate.shape[1]
             desc.fmt = MOE_W_BF16

@@ -38,6 +38,7 @@ moe_status check_shape(const moe_layer_desc *d) {
     if (d->d % 64 || d->I % 64 || d->d > 8192 || d->I > 4096 || d->max_tokens > 65536) return MOE_ERR_UNSUPPORTED;
     if (d->fmt != MOE_W_BF16 && d->fmt != MOE_W_NVFP4) return MOE_ERR_UNSUPPORTED;
     if (d->fmt == MOE_W_NVFP4 && (d->d % 256 || d->I % 256)) return MOE_ERR_UNSUPPORTED;
+    if (d->gate_up_interleaved && d->fmt != MOE_W_BF16) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
 }
 
@@ -46,7 +47,7 @@ moe_status check_desc(const moe_layer_desc *d) {
     if (s != MOE_OK) return s;
     if (!d->w_router || !aligned16(d->w_router)) return MOE_ERR_INVALID_ARG;
     if (d->fmt == MOE_W_BF16) {
-        const void *p[] = {d->w_gate, d->w_up, d->w_down};
+        const void *p[] = {d->w_gate, d->gate_up_interleaved ? d->w_gate : d->w_up, d->w_down};
         for (const void *q : p)
             if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
     } else {
@@ -111,12 +112,14 @@ moe_status forward_prefill(moe_layer *ly, const uint16_t *x, const uint16_t *res
 
 // Which small-batch kernel runs T tokens: the tensor-core layer kernel
 // (decode_mma) or the CUDA-core one (decode_fused). By default the tensor
-// cores take NVFP4 experts and batches of several tokens, where the CUDA
-// cores' arithmetic, not the weight stream, would set the pace.
+// cores take bf16 batches of 8 or more tokens, where the CUDA cores'
+// arithmetic, not the weight stream, sets the pace (measured: 16 tokens 0.87
+// of the HBM roofline on the tensor cores against 0.75; 4 tokens 0.85 on the
+// CUDA cores, whose row-pair stages balance finer than 128-row units).
 bool use_mma(const moe_layer *ly, int T) {
     if (ly->decode_path == MOE_DECODE_CUDA_CORES || !ly->mma_maps_ok || !mma_supported(ly->L, T)) return false;
     if (ly->decode_path == MOE_DECODE_TENSOR_CORES) return true;
-    return ly->L.fmt == MOE_W_NVFP4 || T >= 4;
+    return ly->L.fmt == MOE_W_BF16 && T >= 8;
 }
 
 // Forward on device buffers; res may be NULL.
@@ -217,7 +220,8 @@ moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t 
     L.wr = (const uint16_t *)desc->w_router;
     L.bias = desc->router_bias;
     L.wg = (const uint16_t *)desc->w_gate;
-    L.wu = (const uint16_t *)desc->w_up;
+    L.wu = desc->gate_up_interleaved ? L.wg + desc->d : (const uint16_t *)desc->w_up;
+    L.gu_ld = desc->gate_up_interleaved ? 2 * (int64_t)desc->d : desc->d;
     L.wd = (const uint16_t *)desc->w_down;
     L.qg = desc->q_gate;
     L.qu = desc->q_up;
@@ -384,7 +388,7 @@ moe_status moe_stack_create(moe_layer *const *layers, int n_layers, moe_stack **
         const LayerDev &L = ly->L;
         if (L.d != L0.d || L.E != L0.E || L.k != L0.k || L.I != L0.I || L.fmt != L0.fmt) return MOE_ERR_INVALID_ARG;
         if (L.expert_norm) return MOE_ERR_UNSUPPORTED;
-        w[(size_t)l] = LayerW{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+        w[(size_t)l] = L.weights();
     }
     if (cudaMemcpy(layers[0]->ws.stack, w.data(), sizeof(LayerW) * (size_t)n_layers, cudaMemcpyHostToDevice) !=
         cudaSuccess)

@@ -64,6 +64,7 @@ struct LayerW {
     const uint16_t *wg, *wu, *wd;
     const uint8_t *qg, *qu, *qd, *sg, *su, *sd;
     const float *gg, *gu, *gd;
+    int64_t gu_ld;            // bf16: elements from one gate (or up) row to the next (d, or 2d when interleaved)
 };
 
 // Layers one stacked launch can run.
@@ -395,6 +396,9 @@ struct LayerDev {
     const float *gg, *gu, *gd;
     int num_sms;
     int expert_norm;  // RMS-normalise each expert output before the weighted sum
+    int64_t gu_ld;    // bf16: elements from one gate (or up) row to the next: d, or 2d when the
+                      // rows are interleaved (gate row i, then up row i: wu = wg + d)
+    LayerW weights() const { return LayerW{wr, bias, wg, wu, wd, qg, qu, qd, sg, su, sd, gg, gu, gd, gu_ld}; }
 };
 
 // route.cu

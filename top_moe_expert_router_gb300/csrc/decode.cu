@@ -59,6 +59,7 @@ struct DecodeArgs {
     // slot shared between warps could show a stale phase of the same parity).
     int ncons;
     Workspace ws;
+    int64_t gu_ld;           // elements from one gate (or up) row to the next
 };
 
 // ---------------------------------------------------------------------------
@@ -191,8 +192,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 1) decode_gateup_kernel(Decode
                 unsigned char *dst = ring + (size_t)slot * stage_bytes;
                 mbar_arrive_expect_tx(&full[slot], stage_bytes);
                 if (!FP4) {
-                    bulk_g2s(dst, a.wg + row * d, rb, &full[slot], pol);
-                    bulk_g2s(dst + rb, a.wu + row * d, rb, &full[slot], pol);
+                    bulk_g2s(dst, a.wg + (int64_t)row * a.gu_ld, rb, &full[slot], pol);
+                    bulk_g2s(dst + rb, a.wu + (int64_t)row * a.gu_ld, rb, &full[slot], pol);
                 } else {
                     const uint32_t nq = d / 2, nsb = d / 16;
                     bulk_g2s(dst, a.qg + row * nq, nq, &full[slot], pol);
@@ -480,7 +481,7 @@ static cudaError_t launch_fmt(const LayerDev &L, const DecodeArgs &a, cudaStream
 
 static DecodeArgs make_args(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T) {
     return DecodeArgs{x, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd,
-                      T, L.d, L.I, L.k, 0, 0, ws};
+                      T, L.d, L.I, L.k, 0, 0, ws, L.gu_ld};
 }
 
 cudaError_t launch_decode_gateup(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st) {

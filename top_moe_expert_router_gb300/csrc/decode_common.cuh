@@ -62,6 +62,45 @@ struct Plan {
     __device__ __forceinline__ int dn_unit(int t) const { return t < nC ? c0 + t : offD + d0 + (t - nC); }
 };
 
+// Even shares with the remainders rotated: in segment s (n_s units) every CTA
+// takes n_s / G units and the n_s % G extra ones go to the CTAs from o_s on
+// (cyclically), o_s being where the previous segments' extras ended. So a CTA
+// that took an extra unit in one segment is the last to take one in the next,
+// and the largest share exceeds the mean by at most about one unit overall.
+__device__ __forceinline__ void share_rotated(int total, int b, int G, int o, int &start, int &count) {
+    const int base = total / G, rem = total % G;
+    // extras among CTAs [0, b): those j with (j - o) mod G < rem
+    auto extras_before = [&](int bb) {
+        int n = 0;
+        if (o + rem <= G) {
+            n = min(max(bb - o, 0), rem);
+        } else {
+            n = min(bb, o + rem - G) + min(max(bb - o, 0), G - o);
+        }
+        return n;
+    };
+    start = b * base + extras_before(b);
+    count = base + (((b - o) % G + G) % G < rem ? 1 : 0);
+}
+
+// make_plan with rotated remainders: segments A, B, C, D in that order.
+__device__ __forceinline__ Plan make_plan_rotated(int U, int I, int units_per_expert, int b, int G) {
+    Plan p;
+    const int U1 = (U + 1) / 2, U2 = U - U1;
+    const int nA = U1 * I, nB = U2 * I, nC = U1 * units_per_expert, nD = U2 * units_per_expert;
+    int o = 0;
+    share_rotated(nA, b, G, o, p.a0, p.nA);
+    o = (o + nA % G) % G;
+    share_rotated(nB, b, G, o, p.b0, p.nB);
+    o = (o + nB % G) % G;
+    share_rotated(nC, b, G, o, p.c0, p.nC);
+    o = (o + nC % G) % G;
+    share_rotated(nD, b, G, o, p.d0, p.nD);
+    p.offB = nA;
+    p.offD = nC;
+    return p;
+}
+
 __device__ __forceinline__ Plan make_plan(int U, int I, int units_per_expert, int b, int G) {
     Plan p;
     const int U1 = (U + 1) / 2, U2 = U - U1;

@@ -769,8 +769,14 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                     const size_t row = (size_t)R.uniq[u] * I + i;
                     mbar_arrive_expect_tx(&full[slot], 2 * rbg);
                     if (!FP4) {
-                        bulk_g2s(dst, lw.wg + row * d, rbg, &full[slot], pol);
-                        bulk_g2s(dst + rbg, lw.wu + row * d, rbg, &full[slot], pol);
+                        const int64_t ld = lw.gu_ld;
+                        if (lw.wu == lw.wg + d && ld == 2 * (int64_t)d) {
+                            // interleaved rows: gate row i and up row i are one contiguous copy
+                            bulk_g2s(dst, lw.wg + (int64_t)row * ld, 2 * rbg, &full[slot], pol);
+                        } else {
+                            bulk_g2s(dst, lw.wg + (int64_t)row * ld, rbg, &full[slot], pol);
+                            bulk_g2s(dst + rbg, lw.wu + (int64_t)row * ld, rbg, &full[slot], pol);
+                        }
                     } else {
                         const uint32_t nq = d / 2, nsb = d / 16;
                         bulk_g2s(dst, lw.qg + row * nq, nq, &full[slot], pol);
@@ -1112,7 +1118,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const uint16
     a.x = x;
     a.res = res;
     a.out = out;
-    a.lw0 = LayerW{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+    a.lw0 = L.weights();
     a.n_layers = n_layers;
     a.eps = eps;
     a.layer_out = layer_out;

@@ -34,8 +34,8 @@ bool mma_encode_maps(const LayerDev &L, const LayerW &w, const Workspace &ws, vo
         ok = ok && make_tmap_u8(&m->m[4], w.su, gu_rows, (uint64_t)L.d / 16, 16, kGu);
         ok = ok && make_tmap_u8(&m->m[5], w.sd, dn_rows, (uint64_t)L.I / 16, 16, kDn);
     } else {
-        ok = ok && make_tmap_bf16(&m->m[0], w.wg, gu_rows, (uint64_t)L.d, kGu);
-        ok = ok && make_tmap_bf16(&m->m[1], w.wu, gu_rows, (uint64_t)L.d, kGu);
+        ok = ok && make_tmap_bf16_ld(&m->m[0], w.wg, gu_rows, (uint64_t)L.d, (uint64_t)w.gu_ld, kGu);
+        ok = ok && make_tmap_bf16_ld(&m->m[1], w.wu, gu_rows, (uint64_t)L.d, (uint64_t)w.gu_ld, kGu);
         ok = ok && make_tmap_bf16(&m->m[2], w.wd, dn_rows, (uint64_t)L.I, kDn);
     }
     ok = ok && make_tmap_bf16(&m->m[6], ws.xb, kN, (uint64_t)L.d, kN);
@@ -53,7 +53,7 @@ static cudaError_t launch_t(const LayerDev &L, const Workspace &ws, const TMaps 
     a.x = x;
     a.res = res;
     a.out = out;
-    a.lw0 = LayerW{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+    a.lw0 = L.weights();
     a.n_layers = n_layers;
     a.eps = eps;
     a.layer_out = layer_out;

@@ -402,7 +402,7 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
         fused::route_tokens(R, a.ws.logits, T, k, E, kWarps);
         const int n_uniq = *R.n_uniq;
         if (b == 0) fused::publish_records(R, a.ws, T, k, E, n_uniq, kThreads);
-        const fused::Plan pl = fused::make_plan(n_uniq, I / kGu, d / kDn, b, G);
+        const fused::Plan pl = fused::make_plan_rotated(n_uniq, I / kGu, d / kDn, b, G);
         const int n_gu = pl.nA + pl.nB;
         const int n_units = n_gu + pl.nC + pl.nD;
         const int U1 = (n_uniq + 1) / 2;

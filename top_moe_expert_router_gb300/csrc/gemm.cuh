@@ -244,6 +244,8 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 // 2-D bf16 (or any 2-byte) tensor [rows, K] row-major; box = 64 K-elements x
 // box_rows rows, 128-byte swizzle (the K-major layout the MMA descriptors read).
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows);
+// The same with rows ld elements apart (ld >= K, ld * 2 a multiple of 16).
+bool make_tmap_bf16_ld(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint64_t ld, uint32_t box_rows);
 // 2-D byte tensor [rows, cols] row-major; box = box_cols x box_rows, no swizzle.
 bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
                   uint32_t box_rows);

@@ -191,10 +191,14 @@ bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t col
 
 // 2-D bf16 tensor [rows, K] row-major; box = 64 K-elements x box_rows rows, 128-byte swizzle.
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows) {
+    return make_tmap_bf16_ld(tm, base, rows, K, K, box_rows);
+}
+
+bool make_tmap_bf16_ld(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint64_t ld, uint32_t box_rows) {
     auto enc = get_encode();
     if (!enc) return false;
     cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K * 2};
+    cuuint64_t strides[1] = {ld * 2};
     cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box, estr,
@@ -244,8 +248,8 @@ cudaError_t launch_prefill_experts(const LayerDev &L, const Workspace &ws, const
     const uint64_t rows = (uint64_t)L.max_T * L.k;
     CUtensorMap ta, tg, tu, th, td;
     if (!make_tmap_bf16(&ta, ws.xperm, rows, (uint64_t)L.d, BM) ||
-        !make_tmap_bf16(&tg, L.wg, (uint64_t)L.E * L.I, (uint64_t)L.d, BN / 2) ||
-        !make_tmap_bf16(&tu, L.wu, (uint64_t)L.E * L.I, (uint64_t)L.d, BN / 2) ||
+        !make_tmap_bf16_ld(&tg, L.wg, (uint64_t)L.E * L.I, (uint64_t)L.d, (uint64_t)L.gu_ld, BN / 2) ||
+        !make_tmap_bf16_ld(&tu, L.wu, (uint64_t)L.E * L.I, (uint64_t)L.d, (uint64_t)L.gu_ld, BN / 2) ||
         !make_tmap_bf16(&th, ws.h, rows, (uint64_t)L.I, BM) ||
         !make_tmap_bf16(&td, L.wd, (uint64_t)L.E * L.d, (uint64_t)L.I, BN))
         return cudaErrorInvalidValue;

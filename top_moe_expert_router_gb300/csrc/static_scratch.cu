@@ -58,7 +58,8 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
         !aligned16(desc->w_router))
         return MOE_ERR_INVALID_ARG;
     if (desc->fmt == MOE_W_BF16) {
-        if (!desc->w_gate || !desc->w_up || !desc->w_down || !aligned16(desc->w_gate) || !aligned16(desc->w_up) ||
+        const void *wu = desc->gate_up_interleaved ? desc->w_gate : desc->w_up;
+        if (!desc->w_gate || !wu || !desc->w_down || !aligned16(desc->w_gate) || !aligned16(wu) ||
             !aligned16(desc->w_down))
             return MOE_ERR_INVALID_ARG;
     } else {
@@ -87,7 +88,8 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
     L.wr = (const uint16_t *)desc->w_router;
     L.bias = desc->router_bias;
     L.wg = (const uint16_t *)desc->w_gate;
-    L.wu = (const uint16_t *)desc->w_up;
+    L.wu = desc->gate_up_interleaved ? L.wg + desc->d : (const uint16_t *)desc->w_up;
+    L.gu_ld = desc->gate_up_interleaved ? 2 * (int64_t)desc->d : desc->d;
     L.wd = (const uint16_t *)desc->w_down;
     L.qg = desc->q_gate;
     L.qu = desc->q_up;
