@@ -237,7 +237,7 @@ moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t 
     ly->ws = ws;
     ly->last_launches = 0;
     ly->mma_maps.assign(mma_maps_bytes(), 0);
-    const LayerW w{L.wr, L.bias, L.wg, L.wu, L.wd, L.qg, L.qu, L.qd, L.sg, L.su, L.sd, L.gg, L.gu, L.gd};
+    const LayerW w = L.weights();
     ly->mma_maps_ok = mma_encode_maps(L, w, ws, ly->mma_maps.data());
     *out = ly;
     return MOE_OK;

@@ -34,6 +34,7 @@ bool mma_encode_maps(const LayerDev &L, const LayerW &w, const Workspace &ws, vo
         ok = ok && make_tmap_u8(&m->m[4], w.su, gu_rows, (uint64_t)L.d / 16, 16, kGu);
         ok = ok && make_tmap_u8(&m->m[5], w.sd, dn_rows, (uint64_t)L.I / 16, 16, kDn);
     } else {
+        ok = ok && w.gu_ld >= L.d;   // a row stride below d would alias rows
         ok = ok && make_tmap_bf16_ld(&m->m[0], w.wg, gu_rows, (uint64_t)L.d, (uint64_t)w.gu_ld, kGu);
         ok = ok && make_tmap_bf16_ld(&m->m[1], w.wu, gu_rows, (uint64_t)L.d, (uint64_t)w.gu_ld, kGu);
         ok = ok && make_tmap_bf16(&m->m[2], w.wd, dn_rows, (uint64_t)L.I, kDn);
