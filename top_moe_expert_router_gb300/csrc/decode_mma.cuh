@@ -52,9 +52,9 @@ namespace dmma {
 constexpr int kN = 16;             // MMA N: token columns
 constexpr int kGu = 64;            // gate rows (and up rows) per gate/up unit
 constexpr int kDn = 128;           // W_down rows per down unit
-constexpr int kNAcc = 4;           // accumulators in TMEM, 16 columns each
-constexpr int kNA = 4;             // NVFP4: widened A tiles in TMEM, 32 columns each
-constexpr int kAColBase = kNAcc * kN;   // first TMEM column of the A tiles
+constexpr int kNAcc = 4;           // units in flight between the MMA and the epilogue
+constexpr int kNA = 8;             // NVFP4: widened A tiles in TMEM, 32 columns each
+constexpr int kConvGroups = 2;     // NVFP4: converter groups (4 warps each) taking alternate k-blocks
 constexpr int kMaxSlots = 32;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kFixed = 16 * 1024;  // barriers, routing scratch, exchange buffer
@@ -70,7 +70,15 @@ struct Cfg {
     static constexpr uint32_t kB = kN * 128;                         // 16 rows x 64 K x 2 B
     static constexpr uint32_t kA = FP4 ? 128 * 32 + 128 * 16 : 128 * 128;
     static constexpr uint32_t kStage = kB + kA;                      // 8 KB or 18 KB
-    static constexpr uint32_t kTmemCols = FP4 ? 256 : 64;
+    // A unit's K is split over kKSplit accumulators (k-block kb feeds
+    // accumulator kb % kKSplit; the epilogue adds them): consecutive MMAs into
+    // one N = 16 accumulator wait for each other, so independent chains keep
+    // the tensor pipe busy when a k-block's bytes arrive faster than one chain.
+    static constexpr int kKSplit = FP4 ? 4 : 2;
+    static constexpr int kAccCols = kNAcc * kN * kKSplit;          // accumulators: 256 or 128 columns
+    static constexpr int kAColBase = kAccCols;                     // NVFP4: first column of the A tiles
+    static constexpr uint32_t kTmemCols = FP4 ? 512 : 128;         // + (NVFP4) 8 A tiles x 32 columns
+    static_assert(!FP4 || kAColBase + kNA * 32 <= 512, "tensor memory holds the accumulators and A tiles");
     static_assert(kStage % 1024 == 0, "ring slots stay 1024-byte aligned");
 };
 
@@ -232,10 +240,10 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
     if (tid == 0) {
         for (int s = 0; s < NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1 + C::kConvWarps);   // the MMA's commit + each converter warp
+            mbar_init(&empty[s], 1 + C::kConvWarps / kConvGroups);   // the MMA's commit + the converting group's warps
         }
         for (int s = 0; s < kNA; ++s) {
-            mbar_init(&afull[s], C::kConvWarps > 0 ? C::kConvWarps : 1);
+            mbar_init(&afull[s], C::kConvWarps > 0 ? C::kConvWarps / kConvGroups : 1);
             mbar_init(&aempty[s], 1);
         }
         for (int s = 0; s < kNAcc; ++s) {
@@ -480,9 +488,11 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
                     const int ab = un_mma % kNAcc;
                     if (!mbar_wait_or_abort(&accempty[ab], ((un_mma / kNAcc) & 1) ^ 1, err, abort_flag)) break;
                     tc_fence_after();
-                    const uint32_t dtm = tmem_base + (uint32_t)(ab * kN);
                     const uint32_t idesc = (FP4 && un.gu) ? kIdescF16 : kIdescBf16;
                     for (int kb = 0; kb < un.kbs; ++kb, ++it_mma) {
+                        // partial accumulator kb % kKSplit of unit buffer ab; its first k-block overwrites
+                        const uint32_t dtm = tmem_base + (uint32_t)((ab * C::kKSplit + kb % C::kKSplit) * kN);
+                        const bool first = kb < C::kKSplit;
                         const int slot = it_mma % NS, as = it_mma % kNA;
                         if (!mbar_wait_or_abort(&full[slot], (it_mma / NS) & 1, err, abort_flag) ||
                             (FP4 && !mbar_wait_or_abort(&afull[as], (it_mma / kNA) & 1, err, abort_flag))) {
@@ -496,12 +506,12 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
                             const uint64_t ad = smem_desc_sw128(smem_u32(st + C::kB));
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16(dtm, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0);
+                                mma_bf16(dtm, ad + (uint64_t)(2 * kk), bd + (uint64_t)(2 * kk), idesc, !first || kk != 0);
                         } else {
-                            const uint32_t ta = tmem_base + (uint32_t)(kAColBase + as * 32);
+                            const uint32_t ta = tmem_base + (uint32_t)(C::kAColBase + as * 32);
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_tmem_a(dtm, ta + (uint32_t)(8 * kk), bd + (uint64_t)(2 * kk), idesc, (kb | kk) != 0);
+                                mma_tmem_a(dtm, ta + (uint32_t)(8 * kk), bd + (uint64_t)(2 * kk), idesc, !first || kk != 0);
                         }
                         mma_commit(&empty[slot]);             // slot free once these MMAs have read it
                         if (FP4) mma_commit(&aempty[as]);     // and the widened A tile
@@ -522,8 +532,20 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
                 if (!mbar_wait_or_abort(&accfull[ab], (un_epi / kNAcc) & 1, err, abort_flag)) break;
                 tc_fence_after();
                 uint32_t v[16];
-                tmem_ld16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * kN), v);
-                tmem_ld_wait();
+                {
+                    // the unit's partial accumulators (as many as it had k-blocks, up to kKSplit), added
+                    const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(ab * C::kKSplit * kN);
+                    tmem_ld16(tl, v);
+                    tmem_ld_wait();
+                    const int parts = un.kbs < C::kKSplit ? un.kbs : C::kKSplit;
+                    for (int pp = 1; pp < parts; ++pp) {
+                        uint32_t w[16];
+                        tmem_ld16(tl + (uint32_t)(pp * kN), w);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int t = 0; t < kN; ++t) v[t] = __float_as_uint(__uint_as_float(v[t]) + __uint_as_float(w[t]));
+                    }
+                }
                 tc_fence_before();
                 mbar_arrive(&accempty[ab]);
                 const int n_e = R.cnt[un.e] < kN ? R.cnt[un.e] : kN;
@@ -588,13 +610,16 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
             }
         } else if (FP4) {
             // -------------------------------- converters --------------------------------
+            // group g (4 warps, one per TMEM lane quarter) widens the k-blocks
+            // it with it % 2 == g: two k-blocks are in conversion at once
             const int q = warp & 3;                    // TMEM lane quarter
-            const int hsel = (warp - 6) >> 2;          // which half of the k-block (32 codes)
+            const int grp = (warp - 6) >> 2;
             const int row = q * 32 + lane;             // A row
             bool ok = !*abort_flag;
             for (int n = 0; n < n_units && ok; ++n) {
                 const Unit un = unit_at(pl, R, n, n_gu, d, I);
                 for (int kb = 0; kb < un.kbs; ++kb, ++it_conv) {
+                    if ((it_conv % kConvGroups) != grp) continue;
                     const int slot = it_conv % NS, as = it_conv % kNA;
                     if (!mbar_wait_or_abort(&full[slot], (it_conv / NS) & 1, err, abort_flag) ||
                         !mbar_wait_or_abort(&aempty[as], ((it_conv / kNA) & 1) ^ 1, err, abort_flag)) {
@@ -602,15 +627,20 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
                         break;
                     }
                     const unsigned char *st = ring + (size_t)slot * C::kStage;
-                    const unsigned char *codes = st + C::kB + row * 32 + hsel * 16;
-                    const unsigned char *scales = st + C::kB + 128 * 32 + row * 16 + (kb & 3) * 4 + hsel * 2;
-                    uint32_t o[16];
-                    if (un.gu)
+                    const unsigned char *codes = st + C::kB + row * 32;
+                    const unsigned char *scales = st + C::kB + 128 * 32 + row * 16 + (kb & 3) * 4;
+                    uint32_t o[32];
+                    if (un.gu) {
                         widen32<true>(codes, scales, o);
-                    else
+                        widen32<true>(codes + 16, scales + 2, o + 16);
+                    } else {
                         widen32<false>(codes, scales, o);
+                        widen32<false>(codes + 16, scales + 2, o + 16);
+                    }
                     tc_fence_after();
-                    tmem_st16(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(kAColBase + as * 32 + hsel * 16), o);
+                    const uint32_t ta = tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(C::kAColBase + as * 32);
+                    tmem_st16(ta, o);
+                    tmem_st16(ta + 16, o + 16);
                     tmem_st_wait();
                     tc_fence_before();
                     __syncwarp();
