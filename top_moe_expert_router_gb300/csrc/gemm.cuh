@@ -246,8 +246,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
 bool make_tmap_bf16(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint32_t box_rows);
 // The same with rows ld elements apart (ld >= K, ld * 2 a multiple of 16).
 bool make_tmap_bf16_ld(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t K, uint64_t ld, uint32_t box_rows);
-// 2-D byte tensor [rows, cols] row-major; box = box_cols x box_rows, no swizzle.
+// 2-D byte tensor [rows, cols] row-major; box = box_cols x box_rows, no swizzle
+// (swz32: the 32-byte swizzle, box_cols == 32: in shared memory the two 16-byte
+// halves of row r are swapped when bit 2 of r is set).
 bool make_tmap_u8(CUtensorMap *tm, const void *base, uint64_t rows, uint64_t cols, uint32_t box_cols,
-                  uint32_t box_rows);
+                  uint32_t box_rows, bool swz32 = false);
 
 }  // namespace moe

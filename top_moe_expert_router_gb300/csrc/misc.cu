@@ -15,16 +15,33 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // combine: out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] )
 // ---------------------------------------------------------------------------
-// Four consecutive expert outputs at Y + i (fp32, or bf16 when YT = uint16_t).
-__device__ __forceinline__ float4 load_y4(const float *Y, size_t i) {
-    return __ldcg(reinterpret_cast<const float4 *>(Y + i));
+// CPT consecutive expert outputs at Y + i, widened to fp32 (bf16 outputs:
+// one 16-byte load of 8; fp32 outputs: one 16-byte load of 4).
+template <int CPT>
+__device__ __forceinline__ void load_y(const float *Y, size_t i, float v[CPT]) {
+    static_assert(CPT == 4, "fp32 outputs: 4 columns per thread");
+    const float4 a = __ldcg(reinterpret_cast<const float4 *>(Y + i));
+    v[0] = a.x;
+    v[1] = a.y;
+    v[2] = a.z;
+    v[3] = a.w;
 }
-__device__ __forceinline__ float4 load_y4(const uint16_t *Y, size_t i) {
-    const uint2 v = __ldcg(reinterpret_cast<const uint2 *>(Y + i));
-    return make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+template <int CPT>
+__device__ __forceinline__ void load_y(const uint16_t *Y, size_t i, float v[CPT]) {
+    static_assert(CPT == 8, "bf16 outputs: 8 columns per thread");
+    const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(Y + i));
+    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        v[2 * q] = bf16lo(w[q]);
+        v[2 * q + 1] = bf16hi(w[q]);
+    }
 }
 
-template <typename YT>
+// out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] ), CPT
+// columns per thread; all slot records first, then all expert-output loads
+// (one 16-byte load per slot), then the sum in fp32, j ascending.
+template <typename YT, int CPT>
 __global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, const float *__restrict__ w,
                                                       const int32_t *__restrict__ pos,
                                                       const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
@@ -33,9 +50,8 @@ __global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, 
     // kernels before it
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int t = blockIdx.y;
-    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    const int c = (blockIdx.x * blockDim.x + threadIdx.x) * CPT;
     if (c >= d) return;
-    // all slot records first, then all expert-output loads, then the sum
     float wj[8];
     int rj[8];
 #pragma unroll
@@ -48,31 +64,41 @@ __global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, 
             wj[j] = 0.f;
         }
     }
-    float4 y[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j)
-        y[j] = j < k ? load_y4(Y, (size_t)rj[j] * d + c) : make_float4(0, 0, 0, 0);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float y[8][CPT];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
         if (j < k) {
-            acc.x = fmaf(wj[j], y[j].x, acc.x);
-            acc.y = fmaf(wj[j], y[j].y, acc.y);
-            acc.z = fmaf(wj[j], y[j].z, acc.z);
-            acc.w = fmaf(wj[j], y[j].w, acc.w);
+            load_y<CPT>(Y, (size_t)rj[j] * d + c, y[j]);
+        } else {
+#pragma unroll
+            for (int q = 0; q < CPT; ++q) y[j][q] = 0.f;
         }
     }
+    float acc[CPT];
+#pragma unroll
+    for (int q = 0; q < CPT; ++q) acc[q] = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        if (j < k) {
+#pragma unroll
+            for (int q = 0; q < CPT; ++q) acc[q] = fmaf(wj[j], y[j][q], acc[q]);
+        }
     if (res) {
-        const uint2 rv = *reinterpret_cast<const uint2 *>(res + (size_t)t * d + c);
-        acc.x += bf16lo(rv.x);
-        acc.y += bf16hi(rv.x);
-        acc.z += bf16lo(rv.y);
-        acc.w += bf16hi(rv.y);
+#pragma unroll
+        for (int q = 0; q < CPT; q += 2) {
+            const uint32_t rv = *reinterpret_cast<const uint32_t *>(res + (size_t)t * d + c + q);
+            acc[q] += bf16lo(rv);
+            acc[q + 1] += bf16hi(rv);
+        }
     }
-    uint2 o;
-    o.x = (uint32_t)f32_to_bf16_rn(acc.x) | ((uint32_t)f32_to_bf16_rn(acc.y) << 16);
-    o.y = (uint32_t)f32_to_bf16_rn(acc.z) | ((uint32_t)f32_to_bf16_rn(acc.w) << 16);
-    *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = o;
+    uint32_t o[CPT / 2];
+#pragma unroll
+    for (int q = 0; q < CPT / 2; ++q)
+        o[q] = (uint32_t)f32_to_bf16_rn(acc[2 * q]) | ((uint32_t)f32_to_bf16_rn(acc[2 * q + 1]) << 16);
+    if (CPT == 8)
+        *reinterpret_cast<uint4 *>(out + (size_t)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
+    else
+        *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = make_uint2(o[0], o[1]);
 }
 
 // With per-expert output normalisation: one CTA per token; pass 1 sums the
@@ -165,7 +191,8 @@ cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_
         return cudaLaunchKernelEx(&cfg, combine_norm_kernel, (const float *)ws.Y, (const float *)ws.w,
                                   (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
     }
-    cfg.gridDim = dim3((L.d / 4 + 255) / 256, T);
+    const int cpt = y_bf16 ? 8 : 4;   // columns per thread (d is a multiple of 64)
+    cfg.gridDim = dim3((L.d / cpt + 255) / 256, T);
     cfg.blockDim = dim3(256);
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
@@ -174,9 +201,9 @@ cudaError_t launch_combine(const LayerDev &L, const Workspace &ws, const uint16_
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     if (y_bf16)
-        return cudaLaunchKernelEx(&cfg, combine_kernel<uint16_t>, (const uint16_t *)ws.xperm, (const float *)ws.w,
+        return cudaLaunchKernelEx(&cfg, combine_kernel<uint16_t, 8>, (const uint16_t *)ws.xperm, (const float *)ws.w,
                                   (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
-    return cudaLaunchKernelEx(&cfg, combine_kernel<float>, (const float *)ws.Y, (const float *)ws.w,
+    return cudaLaunchKernelEx(&cfg, combine_kernel<float, 4>, (const float *)ws.Y, (const float *)ws.w,
                               (const int32_t *)ws.pos, res, out, T, L.d, L.k, &ws.ctrl->err, T * L.k);
 }
 

@@ -14,7 +14,7 @@
 //     the B tile's packed E2M1 codes (256 rows x 32 bytes) and the E4M3 block
 //     scales of its rows (16 bytes per row: the scales of 4 k-blocks, of which
 //     this k-block uses 4) into one slot of a 5-deep ring;
-//   * eight converter warps widen the codes: e2m1 pair -> f16 pair (hardware
+//   * eight converter warps (one B row per thread) widen the codes: e2m1 pair -> f16 pair (hardware
 //     conversion), times the block scale in f16 (exact: the product of an
 //     e2m1 and an e4m3 value has at most 6 significant bits and lies in f16's
 //     normal range), optionally -> bf16 (exact likewise), and write the
@@ -53,24 +53,29 @@ constexpr uint32_t kBBytes = BN * BK * 2;         // 32 KB
 constexpr size_t kSmem = 1024 + (size_t)kBStages * kBBytes + (size_t)kQStages * kQStageBytes + 512;
 static_assert(kQStageBytes % 1024 == 0, "A tiles must stay 1024-byte aligned");
 
-// One item of a converter thread: 32 consecutive K elements (half of the
-// k-block) of one B row: 16 code bytes, two block scales.
+// One B row of one k-block, by one converter thread: 64 E2M1 codes (32 bytes,
+// stored with the 32-byte swizzle: the halves swapped when bit 2 of the row is
+// set) times their four block scales (sc: this k-block's 4 E4M3 bytes), widened
+// and written as 8 chunks of 16 bytes at chunk position c ^ (row % 8) of the
+// row's 128 bytes. Eight consecutive rows touch eight different 16-byte bank
+// groups in every access.
 template <bool BF16OUT>
-__device__ __forceinline__ void convert_item(const unsigned char *codes, const unsigned char *scales,
-                                             unsigned char *btile, int row, int half) {
-    const uint4 cw = *reinterpret_cast<const uint4 *>(codes);
-    const uint32_t s2 = e4m3x2_to_f16x2(*reinterpret_cast<const uint16_t *>(scales));
-    const __half2 s = *reinterpret_cast<const __half2 *>(&s2);
-    const __half2 s_lo = __low2half2(s), s_hi = __high2half2(s);   // blocks 2*half, 2*half + 1
-    const uint32_t words[4] = {cw.x, cw.y, cw.z, cw.w};
+__device__ __forceinline__ void convert_row(const unsigned char *codes_tile, uint32_t sc, unsigned char *btile,
+                                            int row) {
+    const int sw = (row >> 2) & 1;
+    const uint4 c0 = *reinterpret_cast<const uint4 *>(codes_tile + row * 32 + (sw << 4));          // codes 0..31
+    const uint4 c1 = *reinterpret_cast<const uint4 *>(codes_tile + row * 32 + ((sw ^ 1) << 4));    // codes 32..63
+    const uint32_t s01 = e4m3x2_to_f16x2((uint16_t)(sc & 0xFFFFu)), s23 = e4m3x2_to_f16x2((uint16_t)(sc >> 16));
+    const __half2 h01 = *reinterpret_cast<const __half2 *>(&s01), h23 = *reinterpret_cast<const __half2 *>(&s23);
+    const __half2 sb[4] = {__low2half2(h01), __high2half2(h01), __low2half2(h23), __high2half2(h23)};
+    const uint32_t words[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const __half2 sj = j < 2 ? s_lo : s_hi;
+    for (int j = 0; j < 8; ++j) {   // word j: codes 8j .. 8j+7, block j / 2
         uint32_t o[4];
         e2m1x8_to_f16x2(words[j], o);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[b]), sj);
+            const __half2 v = __hmul2(*reinterpret_cast<const __half2 *>(&o[b]), sb[j >> 1]);
             if (BF16OUT) {
                 const __nv_bfloat162 bv = __float22bfloat162_rn(__half22float2(v));
                 o[b] = *reinterpret_cast<const uint32_t *>(&bv);
@@ -78,10 +83,7 @@ __device__ __forceinline__ void convert_item(const unsigned char *codes, const u
                 o[b] = *reinterpret_cast<const uint32_t *>(&v);
             }
         }
-        // 16-byte chunk c of the row's 128 bytes, at chunk position c ^ (row % 8)
-        const int c = half * 4 + j;
-        *reinterpret_cast<uint4 *>(btile + (size_t)row * 128 + ((c ^ (row & 7)) << 4)) =
-            make_uint4(o[0], o[1], o[2], o[3]);
+        *reinterpret_cast<uint4 *>(btile + (size_t)row * 128 + ((j ^ (row & 7)) << 4)) = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
@@ -221,9 +223,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // -------------------------------- converters --------------------------------
-        const int ct = threadIdx.x - 192;   // 0 .. kConvThreads - 1
+        const int row = threadIdx.x - 192;   // the B row this thread widens (0 .. 255)
         int it = 0;
         bool ok = true;
+        uint4 sc4 = make_uint4(0, 0, 0, 0);  // the row's scales of 4 k-blocks (read every 4th k-block)
         for (int tile = blockIdx.x; tile < ntiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 const int qs = it % kQStages, bs = it % kBStages;
@@ -233,15 +236,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                     break;
                 }
                 const unsigned char *codes = qring + (size_t)qs * kQStageBytes + kABytes;
-                const unsigned char *scales = codes + kCodeBytes + (kb & 3) * 4;
-                unsigned char *bt = btiles + (size_t)bs * kBBytes;
-#pragma unroll
-                for (int i = 0; i < 2 * BN / kConvThreads; ++i) {   // 512 items: (row, half) of 256 rows
-                    const int item = ct + kConvThreads * i;
-                    const int row = item >> 1, half = item & 1;
-                    convert_item<!F16>(codes + row * (BK / 2) + half * 16, scales + row * kScaleRowBytes + half * 2,
-                                       bt, row, half);
-                }
+                if ((kb & 3) == 0)
+                    sc4 = *reinterpret_cast<const uint4 *>(codes + kCodeBytes + row * kScaleRowBytes);
+                const uint32_t sc = (kb & 3) == 0 ? sc4.x : (kb & 3) == 1 ? sc4.y : (kb & 3) == 2 ? sc4.z : sc4.w;
+                convert_row<!F16>(codes, sc, btiles + (size_t)bs * kBBytes, row);
                 fence_proxy_async_smem();   // these generic-proxy writes, before the MMA (async proxy) reads them
                 __syncwarp();
                 if (lane == 0) {
@@ -339,12 +337,12 @@ cudaError_t launch_prefill_experts_fp4(const LayerDev &L, const Workspace &ws, i
     const uint64_t gu_rows = (uint64_t)L.E * L.I, dn_rows = (uint64_t)L.E * L.d;
     CUtensorMap ta, qg, qu, sg, su, th, qd, sd;
     if (!make_tmap_bf16(&ta, ws.xperm, rows, (uint64_t)L.d, BM) ||
-        !make_tmap_u8(&qg, L.qg, gu_rows, (uint64_t)L.d / 2, BK / 2, BN / 2) ||
-        !make_tmap_u8(&qu, L.qu, gu_rows, (uint64_t)L.d / 2, BK / 2, BN / 2) ||
+        !make_tmap_u8(&qg, L.qg, gu_rows, (uint64_t)L.d / 2, BK / 2, BN / 2, true) ||
+        !make_tmap_u8(&qu, L.qu, gu_rows, (uint64_t)L.d / 2, BK / 2, BN / 2, true) ||
         !make_tmap_u8(&sg, L.sg, gu_rows, (uint64_t)L.d / 16, kScaleRowBytes, BN / 2) ||
         !make_tmap_u8(&su, L.su, gu_rows, (uint64_t)L.d / 16, kScaleRowBytes, BN / 2) ||
         !make_tmap_bf16(&th, ws.h, rows, (uint64_t)L.I, BM) ||
-        !make_tmap_u8(&qd, L.qd, dn_rows, (uint64_t)L.I / 2, BK / 2, BN) ||
+        !make_tmap_u8(&qd, L.qd, dn_rows, (uint64_t)L.I / 2, BK / 2, BN, true) ||
         !make_tmap_u8(&sd, L.sd, dn_rows, (uint64_t)L.I / 16, kScaleRowBytes, BN))
         return cudaErrorInvalidValue;
     GemmParams p{};
