@@ -167,9 +167,11 @@ moe_status moe_debug_route_records(moe_layer *layer, int T, int32_t *ids, float 
                                    int32_t *offsets, int32_t *perm, int32_t *pos, void *stream);
 
 /* Test hook for the device-side failure detection. While hold != 0, every
- * grid barrier of this layer's single-launch decode kernel (T <= 16, and
- * moe_stack_forward on a stack whose first layer is this one) waits for one
- * arrival more than the grid provides, so its bounded wait (1.5 s) runs out:
+ * cross-CTA wait of this layer's single-launch decode kernels (T <= 16, and
+ * moe_stack_forward on a stack whose first layer is this one) waits for
+ * something that never comes: a grid barrier for one arrival more than the
+ * grid provides, the hand-off of the router's logits for a tag no CTA
+ * writes. Its bounded wait (1.5 s) runs out:
  * the launch unwinds without computing the experts, leaves `out` undefined
  * and sets the timeout bit that moe_get_device_status() reports as
  * MOE_ERR_TIMEOUT. hold = 0 restores normal operation; the next call runs

@@ -207,7 +207,7 @@ moe_status moe_layer_create(const moe_layer_desc *desc, void *workspace, size_t 
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return MOE_ERR_CUDA;
-    if (cudaMemset(ws.ctrl, 0, sizeof(Control)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemset(ws.ctrl, 0, control_bytes(ws, desc->E)) != cudaSuccess) return MOE_ERR_CUDA;
     moe_layer *ly = new (std::nothrow) moe_layer();
     if (!ly) return MOE_ERR_INVALID_ARG;
     LayerDev &L = ly->L;

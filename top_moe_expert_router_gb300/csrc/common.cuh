@@ -38,7 +38,8 @@ struct Control {
     int32_t n_tiles_gu;      // prefill: gate/up tiles
     int32_t n_tiles_dn;      // prefill: down tiles
     uint32_t test_hold;      // test hook: arrivals the decode kernel's grid barriers wait for beyond the grid (0)
-    uint32_t pad0[26];
+    uint32_t epoch;          // small-batch decode kernel: tag base of the launch's logits (advanced by the last CTA out)
+    uint32_t pad0[25];
     CtrLine grid_bar;        // fused decode kernel: grid-barrier arrivals (reset by the last CTA out)
     CtrLine grid_exit;       // fused decode kernel: CTAs that finished
     CtrLine h_ready[2];      // fused decode kernel: h rows written, first / second half of the experts
@@ -74,6 +75,7 @@ struct Workspace {
     Control *ctrl;
     LayerW *stack;      // [kMaxStack] weights of the layers of a stacked launch
     float *logits;      // [kRouterSplit][max_T, E] (decode: the first slice)
+    uint64_t *tlogits;  // [16, E] small-batch decode: tagged logits (fp32 logit | tag << 32), zeroed at set-up
     int32_t *ids;       // [max_T, k]
     float *w;           // [max_T, k]
     int32_t *counts;    // [E]
@@ -123,6 +125,7 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     };
     size_t Tk = (size_t)max_T * k;
     ws.ctrl = (Control *)take(sizeof(Control));
+    ws.tlogits = (uint64_t *)take(sizeof(uint64_t) * 16 * (size_t)E);   // right after ctrl: one memset clears both
     ws.stack = (LayerW *)take(sizeof(LayerW) * kMaxStack);
     ws.logits = (float *)take(sizeof(float) * (size_t)kRouterSplit * max_T * E);
     ws.ids = (int32_t *)take(sizeof(int32_t) * Tk);
@@ -147,6 +150,12 @@ inline Workspace workspace_layout(void *base, int d, int E, int k, int I, int ma
     ws.chunk_bm = (uint32_t *)take(sizeof(uint32_t) * nchunks * E);
     ws.bytes = off;
     return ws;
+}
+
+// Bytes from ws.ctrl to the end of ws.tlogits (E experts): the control words
+// and the tagged logits, cleared together at set-up.
+inline size_t control_bytes(const Workspace &ws, int E) {
+    return (size_t)((const char *)ws.tlogits - (const char *)ws.ctrl) + sizeof(uint64_t) * 16 * (size_t)E;
 }
 
 // ---------------------------------------------------------------------------

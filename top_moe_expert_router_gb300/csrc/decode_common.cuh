@@ -1,8 +1,8 @@
 // decode_common.cuh — pieces shared by the two persistent small-batch layer
 // kernels (decode_fused.cuh: experts on CUDA cores; decode_mma.cuh: experts on
 // the tensor cores): acquire loads, the bounded grid barrier, even shares,
-// the h-row hand-off counters, and the routing of up to 16 tokens computed in
-// shared memory by every CTA.
+// the h-row hand-off counters, the tagged logits, and the routing of up to 16
+// tokens computed in shared memory by every CTA.
 #pragma once
 
 #include "common.cuh"
@@ -45,9 +45,16 @@ __device__ inline bool grid_barrier(uint32_t *ctr, uint32_t target, uint32_t *er
     return ok != 0;
 }
 
+// n / dv for 0 <= n < 2^63, dv > 0, in 32-bit arithmetic whenever n fits
+// (every share of these kernels' unit counts does; a 64-bit division is a
+// long software sequence on the prologue's critical path).
+__device__ __forceinline__ long long div_u(long long n, int dv) {
+    return (unsigned long long)n < 0x100000000ull ? (long long)((uint32_t)n / (uint32_t)dv) : n / dv;
+}
+
 __device__ __forceinline__ void share(int total, int b, int G, int &start, int &count) {
-    start = (int)((long long)b * total / G);
-    count = (int)((long long)(b + 1) * total / G) - start;
+    start = (int)div_u((long long)b * total, G);
+    count = (int)div_u((long long)(b + 1) * total, G) - start;
 }
 
 // This CTA's stages: segment A = first-half gate/up row pairs, B = second-half
@@ -143,111 +150,214 @@ struct Route {
     int32_t *ids, *pos, *perm, *cnt, *off, *uniq, *scan;
     float *w;
     uint32_t *bm;
+    uint32_t *wsum;    // [8] per-warp totals of the routing scan
     int *n_uniq;
 };
 
-// exclusive scan of a[0..n) (n <= 256) by one warp; returns the total
-__device__ inline int warp_scan256(const int32_t *a, int32_t *out, int n) {
-    const int lane = threadIdx.x & 31;
-    int vals[8], local = 0;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        vals[i] = idx < n ? a[idx] : 0;
-        local += vals[i];
-    }
-    int incl = local;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
-        if (lane >= o) incl += y;
-    }
-    int run = incl - local;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int idx = lane * 8 + i;
-        if (idx < n) out[idx] = run;
-        run += vals[i];
-    }
-    return __shfl_sync(0xFFFFFFFFu, incl, 31);
+// Logits of the small-batch router handed from CTA to CTA without a grid
+// barrier: each is one 64-bit word, the fp32 logit in the low half and a tag
+// in the high half. The word is stored and loaded whole (single-copy atomic),
+// so a reader that sees the tag it expects holds that launch's logit; no
+// fence or counter is involved. The tag is the layer's epoch (see
+// decode_fused.cuh), different from every tag an earlier launch left behind.
+__device__ __forceinline__ void st_tagged(uint64_t *p, float v, uint32_t tag) {
+    const uint64_t w = ((uint64_t)tag << 32) | (uint64_t)__float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
 }
 
+__device__ __forceinline__ void ld_tagged2(const uint64_t *p, uint64_t &a, uint64_t &b) {
+    asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
 
-// Routing of T <= 16 tokens in shared memory, by every CTA of the launch (the
-// logits of all tokens are complete in global memory): warp w takes tokens
-// w, w + nwarps, ...: top-k, weights; then one warp builds the permutation:
-// experts ascending, tokens ascending within an expert (one token: its k
-// distinct experts, ascending, are its k rows). Ends with __syncthreads().
-__device__ __forceinline__ void route_tokens(const Route &R, const float *logits, int T, int k, int E, int nwarps) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    for (int t = warp; t < T; t += nwarps)
-        topk_warp(logits + (size_t)t * E, E, k, R.ids + t * k, R.w + t * k, true);
-    if (T > 1) __syncthreads();  // one token: warp 0 picked its experts itself
-    if (warp == 0 && T == 1) {
-        // one token: its k distinct experts, ascending, are the k rows
-        __syncwarp();
-        const int my = lane < k ? R.ids[lane] : 0x7FFFFFFF;
-        int rank = 0;
-        int cnt_i[8], off_i[8];
+// A real expert's order key, never 0 (0 marks an empty place: an expert id
+// >= E, or one already picked). Only the one NaN bit pattern whose key would
+// be 0 moves up by one.
+__device__ __forceinline__ uint32_t expert_key(float f) {
+    const uint32_t kk = order_key(f);
+    return kk ? kk : 1u;
+}
+
+// This lane's eight keys, experts 8 * lane + i, from a plain fp32 logits row
+// (written by other CTAs before a grid barrier: read through L2).
+__device__ __forceinline__ void lane_keys(const float *row, int E, uint32_t key[8]) {
+    const int lane = threadIdx.x & 31;
+    const int e0 = 8 * lane;
+    if ((E & 7) == 0 && e0 < E) {
+        const float4 a = __ldcg(reinterpret_cast<const float4 *>(row + e0));
+        const float4 b = __ldcg(reinterpret_cast<const float4 *>(row + e0) + 1);
+        const float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) cnt_i[i] = off_i[i] = 0;
-        for (int q = 0; q < k; ++q) {
-            const int o = __shfl_sync(0xFFFFFFFFu, my, q);
-            rank += o < my;
+        for (int i = 0; i < 8; ++i) key[i] = expert_key(v[i]);
+    } else {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                const int e = lane + 32 * i;
-                cnt_i[i] += o == e;
-                off_i[i] += o < e;
+        for (int i = 0; i < 8; ++i) key[i] = e0 + i < E ? expert_key(__ldcg(row + e0 + i)) : 0u;
+    }
+}
+
+// The same from a row of tagged logits, polling until every word of the
+// warp's row carries `tag` (bounded: on timeout the error word gets
+// ERRBIT_TIMEOUT, the CTA's abort flag is set and whatever was read is used).
+__device__ __forceinline__ void lane_keys_tagged(const uint64_t *row, int E, uint32_t tag, uint32_t key[8],
+                                                 uint32_t *err, volatile int *abort_flag) {
+    const int lane = threadIdx.x & 31;
+    const int e0 = 8 * lane;
+    uint64_t w[8];
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        bool ok = true;
+        if ((E & 7) == 0) {
+            if (e0 < E) {
+#pragma unroll
+                for (int i = 0; i < 8; i += 2) ld_tagged2(row + e0 + i, w[i], w[i + 1]);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                if (e0 + i < E) w[i] = *reinterpret_cast<const volatile uint64_t *>(row + e0 + i);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) ok = ok && (e0 + i >= E || (uint32_t)(w[i] >> 32) == tag);
+        if (__all_sync(0xFFFFFFFFu, ok)) break;
+        if ((it & 63u) == 63u) {
+            const unsigned long long now = global_ns();
+            if (t0 == 0) t0 = now;
+            const bool give_up = *abort_flag != 0 || now - t0 > kWaitLimitNs;
+            if (__any_sync(0xFFFFFFFFu, give_up)) {
+                if (lane == 0) {
+                    atomicOr(err, ERRBIT_TIMEOUT);
+                    *abort_flag = 1;
+                }
+                break;
             }
         }
+    }
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E) {
-                R.cnt[e] = cnt_i[i];
-                R.off[e] = off_i[i];
+    for (int i = 0; i < 8; ++i) key[i] = e0 + i < E ? expert_key(__uint_as_float((uint32_t)w[i])) : 0u;
+}
+
+// Top-k (k <= 8) of one token from the warp's keys (lane l: experts 8l .. 8l+7,
+// 0 for empty places): ids by descending logit, ties to the lower id; weights
+// exp(l - l_max) / sum over the kept, summed in pick order (the same
+// arithmetic as topk_warp). Each lane first sorts its eight (key, id) pairs
+// (descending key, ascending id among equal keys; a 19-comparator network),
+// so a pick is one warp-wide max of the lanes' heads: among the lanes whose
+// head reaches it the lowest lane holds the lowest id, since lane l's ids all
+// lie below lane l+1's. The winning lane stores the id and drops its head.
+__device__ __forceinline__ void topk_sorted(uint32_t key[8], int k, int32_t *ids_out, float *w_out) {
+    const int lane = threadIdx.x & 31;
+    int id[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) id[i] = 8 * lane + i;
+    auto ce = [&](int a, int b) {
+        const bool sw = key[b] > key[a] || (key[b] == key[a] && id[b] < id[a]);
+        const uint32_t ka = sw ? key[b] : key[a], kb = sw ? key[a] : key[b];
+        const int ia = sw ? id[b] : id[a], ib = sw ? id[a] : id[b];
+        key[a] = ka;
+        key[b] = kb;
+        id[a] = ia;
+        id[b] = ib;
+    };
+    ce(0, 2); ce(1, 3); ce(4, 6); ce(5, 7);
+    ce(0, 4); ce(1, 5); ce(2, 6); ce(3, 7);
+    ce(0, 1); ce(2, 3); ce(4, 5); ce(6, 7);
+    ce(2, 4); ce(3, 5);
+    ce(1, 4); ce(3, 6);
+    ce(1, 2); ce(3, 4); ce(5, 6);
+    uint32_t my_key = 0u;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        if (j < k) {
+            const uint32_t m = __reduce_max_sync(0xFFFFFFFFu, key[0]);
+            const uint32_t bal = __ballot_sync(0xFFFFFFFFu, key[0] == m);
+            if (lane == j) my_key = m;
+            if (lane == __ffs(bal) - 1) {
+                ids_out[j] = id[0];
+#pragma unroll
+                for (int i = 0; i < 7; ++i) {
+                    key[i] = key[i + 1];
+                    id[i] = id[i + 1];
+                }
+                key[7] = 0u;
             }
         }
-        if (lane < k) {
-            R.uniq[rank] = my;
-            R.perm[rank] = 0;
-            R.pos[lane] = rank;
+    }
+    const float lmax = __shfl_sync(0xFFFFFFFFu, key_value(my_key), 0);
+    const float ex = lane < k ? expf(key_value(my_key) - lmax) : 0.f;
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, ex, j);
+    if (lane < k) w_out[lane] = ex / sum;
+}
+
+// Routing of T <= 16 tokens in shared memory, by every CTA of the launch (all
+// blockDim.x >= 256 threads take part; E <= 256, k <= 8):
+//  1. warp w takes tokens w, w + nwarps, ...: top-k and weights (from the
+//     tagged logits when `tlogits` is set, else from the plain fp32 rows);
+//  2. one thread per (token, pick) sets the token's bit in its expert's bitmap;
+//  3. one scan over the experts of (count, used) gives each expert's first
+//     row (offsets), the used experts ascending (uniq) and, at uniq index u,
+//     the rows before expert uniq[u] (R.scan: the prefix of the experts'
+//     token counts, n_uniq + 1 entries);
+//  4. one thread per (token, pick) places it: experts ascending, tokens
+//     ascending within an expert.
+// Ends with __syncthreads().
+__device__ __forceinline__ void route_tokens(const Route &R, const float *logits, const uint64_t *tlogits,
+                                             uint32_t tag, int T, int k, int E, uint32_t *err,
+                                             volatile int *abort_flag) {
+    const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    for (int e = tid; e < 256; e += nthr) R.bm[e] = 0u;
+    for (int t = warp; t < T; t += nwarps) {
+        uint32_t key[8];
+        if (tlogits)
+            lane_keys_tagged(tlogits + (size_t)t * E, E, tag, key, err, abort_flag);
+        else
+            lane_keys(logits + (size_t)t * E, E, key);
+        topk_sorted(key, k, R.ids + t * k, R.w + t * k);
+    }
+    __syncthreads();
+    for (int p = tid; p < T * k; p += nthr) {
+        const int e = R.ids[p];
+        if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
+    }
+    __syncthreads();
+    // (count, used) packed in one word: counts sum to <= T * k <= 128 and
+    // the used experts number <= 256, so neither half carries into the other
+    uint32_t v = 0u, inc = 0u;
+    int c = 0;
+    if (tid < 256) {
+        c = tid < E ? __popc(R.bm[tid]) : 0;
+        v = (uint32_t)c | ((c > 0 ? 1u : 0u) << 16);
+        inc = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+            if (lane >= o) inc += y;
         }
-        if (lane == 0) {
-            R.off[E] = k;
-            *R.n_uniq = k;
+        if (lane == 31) R.wsum[warp] = inc;
+    }
+    __syncthreads();
+    if (tid < 256) {
+        uint32_t pre = 0u;
+        for (int i = 0; i < warp; ++i) pre += R.wsum[i];
+        const uint32_t ex = pre + inc - v;
+        if (tid < E) {
+            R.cnt[tid] = c;
+            R.off[tid] = (int)(ex & 0xFFFFu);
+            if (c > 0) {
+                R.uniq[ex >> 16] = tid;
+                R.scan[ex >> 16] = (int)(ex & 0xFFFFu);
+            }
         }
-    } else if (warp == 0) {
-        // the permutation (at most 16 x 8 pairs) by one warp: experts ascending,
-        // tokens ascending within an expert
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) R.bm[e] = 0u;
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
-            if ((unsigned)e < (unsigned)E) atomicOr(&R.bm[e], 1u << (p / k));
+        if (tid == 255) {
+            const uint32_t tot = pre + inc;
+            R.off[E] = (int)(tot & 0xFFFFu);
+            R.scan[tot >> 16] = (int)(tot & 0xFFFFu);
+            *R.n_uniq = (int)(tot >> 16);
         }
-        __syncwarp();
-        for (int e = lane; e < E; e += 32) {
-            const int c = __popc(R.bm[e]);
-            R.cnt[e] = c;
-            R.scan[e] = c > 0;
-        }
-        __syncwarp();
-        const int total = warp_scan256(R.cnt, R.off, E);
-        __syncwarp();
-        const int nu = warp_scan256(R.scan, R.scan, E);
-        __syncwarp();
-        for (int e = lane; e < E; e += 32)
-            if (R.cnt[e] > 0) R.uniq[R.scan[e]] = e;
-        if (lane == 0) {
-            R.off[E] = total;
-            *R.n_uniq = nu;
-        }
-        __syncwarp();
-        for (int p = lane; p < T * k; p += 32) {
-            const int e = R.ids[p];
+    }
+    __syncthreads();
+    for (int p = tid; p < T * k; p += nthr) {
+        const int e = R.ids[p];
+        if ((unsigned)e < (unsigned)E) {
             const int t = p / k;
             const int row = R.off[e] + __popc(R.bm[e] & ((1u << t) - 1u));
             R.perm[row] = t;

@@ -7,11 +7,12 @@
 // ("How SGLang-TorchTPU accelerated an 816B-parameter MoE on TPU v7",
 // sections "Introduction" and "Key optimisations"). Here the layer is one
 // cooperative launch, one CTA per SM:
-//   1. router: every CTA computes the logits of its experts (x . Wr[e]),
-//      grid barrier;
-//   2. routing: every CTA computes top-k and the permutation of all T tokens
-//      itself, in shared memory (identical results everywhere; CTA 0 also
-//      publishes them), so no second barrier is needed;
+//   1. router: every CTA computes the logits of its experts (x . Wr[e]) and
+//      stores each as one 64-bit word with the layer's tag;
+//   2. routing: every CTA reads all logits, waiting for each word's tag (no
+//      grid barrier: the tag is the hand-off), and computes top-k and the
+//      permutation of all T tokens itself, in shared memory (identical
+//      results everywhere; CTA 0 also publishes them);
 //   3. producer lanes (polling, never blocking) fill a ring of shared-memory
 //      slots with bulk TMA copies: first this CTA's share of the active
 //      experts' gate/up rows, then, without a pause, its share of their down
@@ -25,8 +26,12 @@
 //   5. combine: per 256-column block of the output, the CTA whose down rows
 //      complete the block (a row counter per block) forms
 //      out = (res +) sum_j w_j Y_j for those columns, in fp32, j ascending.
-// Every wait (mbarrier, grid barrier) is bounded; a timeout sets the error
-// word and the kernel unwinds. With STACK the kernel loops over layers
+// Every wait (mbarrier, tag, h count, grid barrier) is bounded; a timeout
+// sets the error word and the kernel unwinds. The tags: the control block's
+// epoch, read at entry, gives layer l the tag epoch + 1 + l, and the last CTA
+// out advances the epoch by the launch's layer count, so no word left by an
+// earlier launch carries a tag a later one waits for (every launch rewrites
+// all 16 rows; set-up clears the words and the epoch together). With STACK the kernel loops over layers
 // (decode_stack.cu): each layer's input is RMSNorm of the previous output,
 // computed in every CTA, and a grid barrier separates the layers.
 #pragma once
@@ -57,6 +62,7 @@ constexpr int kDnRows = 4;                    // down rows per stage
 constexpr int kMaxSlots = 32;
 constexpr int kSmemBudget = 227 * 1024;
 constexpr int kCb = 256;                      // output columns per combine block
+constexpr int kTagRows = 16;                  // token rows of the tagged logits (every row, every layer)
 
 struct Args {
     const uint16_t *x;        // [T, d] bf16 (stacked: the first layer's input)
@@ -113,21 +119,20 @@ __device__ __forceinline__ float e4m3f(uint8_t s) {
     return __half2float(*reinterpret_cast<__half *>(&hr));
 }
 
-// Cost of one stage of an expert with n tokens, in arbitrary units: every
-// stage streams the same bytes, but in a multi-token batch the arithmetic,
-// which grows with the tokens, sets the pace. Measured at 4 and 16 tokens
-// (costs 2 + n, 1 + n, 1 + 2n, n and a steeper 3n tried), n balances best.
-__device__ __forceinline__ int stage_weight(int n) { return n; }
-
 // Index, within a segment of experts [u_lo, u_hi) holding `per` stages each,
 // where CTA bb's share starts when the segment is cut into G parts of equal
 // total weight (bb = G gives the segment's end). cw: exclusive prefix over
-// experts of one stage's weight.
+// experts of one stage's weight. A stage of an expert with n tokens weighs n:
+// every stage streams the same bytes, but in a multi-token batch the
+// arithmetic, which grows with the tokens, sets the pace (measured at 4 and
+// 16 tokens, stage costs 2 + n, 1 + n, 1 + 2n, n and 3n tried: n balances
+// best). So cw is the prefix of the experts' token counts, which the routing
+// leaves in R.scan.
 __device__ __forceinline__ int weighted_start(const int32_t *cw, int u_lo, int u_hi, int per, int bb, int G) {
     if (u_hi <= u_lo) return 0;
     if (bb >= G) return (u_hi - u_lo) * per;
     const long long base = cw[u_lo];
-    const long long t = (long long)(cw[u_hi] - base) * per * bb / G;
+    const long long t = div_u((long long)(cw[u_hi] - base) * per * bb, G);
     int lo = u_lo, hi = u_hi;  // the expert holding weight position t
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -137,26 +142,8 @@ __device__ __forceinline__ int weighted_start(const int32_t *cw, int u_lo, int u
             hi = mid;
     }
     const long long w = cw[lo + 1] - cw[lo];
-    const long long j = (t - (long long)(cw[lo] - base) * per + w - 1) / w;
+    const long long j = div_u(t - (long long)(cw[lo] - base) * per + w - 1, (int)w);
     return (lo - u_lo) * per + (int)(j < per ? j : per);
-}
-
-// make_plan with the segments cut by weight instead of by stage count.
-__device__ __forceinline__ Plan make_plan_weighted(const int32_t *cw, int U, int I, int units_per_expert, int b,
-                                                   int G) {
-    Plan p;
-    const int U1 = (U + 1) / 2;
-    p.a0 = weighted_start(cw, 0, U1, I, b, G);
-    p.nA = weighted_start(cw, 0, U1, I, b + 1, G) - p.a0;
-    p.b0 = weighted_start(cw, U1, U, I, b, G);
-    p.nB = weighted_start(cw, U1, U, I, b + 1, G) - p.b0;
-    p.c0 = weighted_start(cw, 0, U1, units_per_expert, b, G);
-    p.nC = weighted_start(cw, 0, U1, units_per_expert, b + 1, G) - p.c0;
-    p.d0 = weighted_start(cw, U1, U, units_per_expert, b, G);
-    p.nD = weighted_start(cw, U1, U, units_per_expert, b + 1, G) - p.d0;
-    p.offB = U1 * I;
-    p.offD = U1 * units_per_expert;
-    return p;
 }
 
 // Sums of four rows' per-lane partials (one token), reduced together:
@@ -495,6 +482,9 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     const int G = gridDim.x, b = blockIdx.x;
     uint32_t *err = &a.ws.ctrl->err;
     Control *ctrl = a.ws.ctrl;
+    // the launch's epoch: layer l's logits carry the tag ep0 + 1 + l; the last
+    // CTA out advances the epoch past this launch's tags
+    const uint32_t ep0 = *reinterpret_cast<const volatile uint32_t *>(&ctrl->epoch);
 
     // ---- shared-memory layout ----
     uint64_t *full = reinterpret_cast<uint64_t *>(smem);
@@ -518,6 +508,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     R.pos = R.ids + 128;                            // [16 * 8]
     R.perm = R.pos + 128;                           // [16 * 8]
     R.w = reinterpret_cast<float *>(R.perm + 128);  // [16 * 8]
+    R.wsum = reinterpret_cast<uint32_t *>(R.w + 128);       // [8]
     R.n_uniq = n_uniq_s;
     unsigned char *xs = smem + 2048 + 8192;
     const uint32_t x_bytes = a.x_in_smem ? (uint32_t)T * d * 2 : 0u;
@@ -640,7 +631,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                 wpre[j] = (mine && v < nq) ? __ldg(wrow + v) : make_uint4(0, 0, 0, 0);
             }
             if (!x_ready) {
-                mbar_wait_or_abort(xbar, 0, err, abort_flag);  // a timeout unwinds at the grid barrier below
+                mbar_wait_or_abort(xbar, 0, err, abort_flag);  // a timeout: the routing's tag wait gives up at once
                 x_ready = true;
             }
             if (mine) {
@@ -671,21 +662,25 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
                 if (lane == 0 && warp < 8) part[warp * TM + t] = s;
             }
             __syncthreads();
-            if (tid < 2 * TM) {
-                const int half = tid / TM, t = tid % TM;
+            if (tid < 2 * kTagRows) {
+                // every row of the tagged logits (rows past T hold 0), so each
+                // word read later was written by this launch or the previous one
+                const int half = tid / kTagRows, t = tid % kTagRows;
                 const int e2 = base + half * G;
-                if (e2 < E && t < T) {
-                    const float *pp = part + half * 4 * TM;
-                    float l = ((pp[0 * TM + t] + pp[1 * TM + t]) + pp[2 * TM + t]) + pp[3 * TM + t];
-                    if (lw.bias) l += lw.bias[e2];
-                    a.ws.logits[(size_t)t * E + e2] = l;
+                if (e2 < E) {
+                    float l = 0.f;
+                    if (t < T) {
+                        const float *pp = part + half * 4 * TM;
+                        l = ((pp[0 * TM + t] + pp[1 * TM + t]) + pp[2 * TM + t]) + pp[3 * TM + t];
+                        if (lw.bias) l += lw.bias[e2];
+                    }
+                    st_tagged(a.ws.tlogits + (size_t)t * E + e2, l, ep0 + 1u + (uint32_t)layer);
                 }
             }
             __syncthreads();
         }
         if (!x_ready) mbar_wait_or_abort(xbar, 0, err, abort_flag);  // CTAs without router rows
     }
-    grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 1) * G, err, abort_flag, &ctrl->test_hold);
 
     if (FP4 && x_bytes) {
         // NVFP4 gate/up sums in fp16: keep the staged tokens as fp16(x / max|x|)
@@ -712,7 +707,13 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     }
 
     // ---- 2. routing, computed by every CTA in shared memory ----
-    route_tokens(R, a.ws.logits, T, k, E, kConsumers + 1);
+    // (the logits come from every CTA's router: each word is waited for by
+    // its tag, so no grid barrier stands between the router and the routing;
+    // the test hook shifts the awaited tag to one that never comes)
+    {
+        const uint32_t hold = *reinterpret_cast<const volatile uint32_t *>(&ctrl->test_hold);
+        route_tokens(R, nullptr, a.ws.tlogits, ep0 + 1u + (uint32_t)layer + hold, T, k, E, err, abort_flag);
+    }
     const int n_uniq = *R.n_uniq;
     if (b == 0) publish_records(R, a.ws, T, k, E, n_uniq, kThreads);
 
@@ -730,16 +731,25 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     if (T == 1) {
         pl = make_plan(n_uniq, I, d / kDnRows, b, G);
     } else {
-        int32_t *cw = R.scan;  // free after the permutation
-        int32_t *wt = reinterpret_cast<int32_t *>(R.bm);
-        if (warp == 0) {
-            for (int u = lane; u < n_uniq; u += 32) wt[u] = stage_weight(min(R.cnt[R.uniq[u]], TM));
-            __syncwarp();
-            const int total = warp_scan256(wt, cw, n_uniq);
-            if (lane == 0) cw[n_uniq] = total;
+        // the segments cut by weight: the eight cut points, one thread each
+        int *cut = reinterpret_cast<int *>(R.wsum);   // free after the routing
+        const int U1h = (n_uniq + 1) / 2;
+        if (tid < 8) {
+            const int sg = tid >> 1;   // A, B, C, D
+            const int lo = (sg & 1) ? U1h : 0, hi = (sg & 1) ? n_uniq : U1h;
+            cut[tid] = weighted_start(R.scan, lo, hi, sg < 2 ? I : d / kDnRows, b + (tid & 1), G);
         }
         __syncthreads();
-        pl = make_plan_weighted(cw, n_uniq, I, d / kDnRows, b, G);
+        pl.a0 = cut[0];
+        pl.nA = cut[1] - cut[0];
+        pl.b0 = cut[2];
+        pl.nB = cut[3] - cut[2];
+        pl.c0 = cut[4];
+        pl.nC = cut[5] - cut[4];
+        pl.d0 = cut[6];
+        pl.nD = cut[7] - cut[6];
+        pl.offB = U1h * I;
+        pl.offD = U1h * (d / kDnRows);
     }
     const int n_gu = pl.nA + pl.nB;
     const int n_st = n_gu + pl.nC + pl.nD;
@@ -1080,7 +1090,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
             hbase[0] += (uint32_t)(U1 * I);
             hbase[1] += (uint32_t)((n_uniq - U1) * I);
         }
-        grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 2) * G, err, abort_flag, &ctrl->test_hold);
+        grid_barrier(&ctrl->grid_bar.v, (uint32_t)(layer + 1) * G, err, abort_flag, &ctrl->test_hold);
     }
     }  // layers
     // ---- exit: the last CTA out resets the grid-barrier counters ----
@@ -1093,6 +1103,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
             ctrl->h_ready[0].v = 0u;
             ctrl->h_ready[1].v = 0u;
             ctrl->grid_exit.v = 0u;
+            ctrl->epoch = ep0 + (uint32_t)(STACK ? a.n_layers : 1);
             fence_acq_rel_gpu();
         }
     }

@@ -232,6 +232,7 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
     R.pos = R.ids + 128;
     R.perm = R.pos + 128;
     R.w = reinterpret_cast<float *>(R.perm + 128);
+    R.wsum = reinterpret_cast<uint32_t *>(R.w + 128);
     R.n_uniq = reinterpret_cast<int *>(smem + 784);
     float *xch = reinterpret_cast<float *>(smem + 11264);          // [64 rows][16] up values (4 KB)
     unsigned char *ring = smem + kFixed;
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
         fused::grid_barrier(&ctrl->grid_bar.v, (uint32_t)(2 * layer + 1) * G, err, abort_flag, &ctrl->test_hold);
 
         // ---- 2. routing, in every CTA ----
-        fused::route_tokens(R, a.ws.logits, T, k, E, kWarps);
+        fused::route_tokens(R, a.ws.logits, nullptr, 0u, T, k, E, err, abort_flag);
         const int n_uniq = *R.n_uniq;
         if (b == 0) fused::publish_records(R, a.ws, T, k, E, n_uniq, kThreads);
         const fused::Plan pl = fused::make_plan_rotated(n_uniq, I / kGu, d / kDn, b, G);

@@ -106,8 +106,9 @@ extern "C" moe_status moe_forward_static_scratch(const moe_layer_desc *desc, con
 
     cudaStream_t st = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the control words (error
-    // bits, the router's arrival counter) must start at zero
-    if (cudaMemsetAsync(ws.ctrl, 0, sizeof(Control), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // bits, counters, the logits' epoch) and the tagged logits start at zero
+    // (with the epoch back at 0, a tag left by an earlier call could match)
+    if (cudaMemsetAsync(ws.ctrl, 0, control_bytes(ws, L.E), st) != cudaSuccess) return MOE_ERR_CUDA;
     // the same single-launch layer kernel moe_forward runs for T <= 16
     const cudaError_t e = launch_decode_fused(L, ws, (const uint16_t *)x, nullptr, (uint16_t *)out, T, st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
