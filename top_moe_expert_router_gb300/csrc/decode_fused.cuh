@@ -268,7 +268,8 @@ __device__ __forceinline__ void gu_stage(const Args &a, const LayerW &lw, const 
         if (a.x_in_smem) {
             // tokens in shared memory as fp16(x / max|x|): the 16 products
             // of a block (|e2m1| <= 6, |x'| <= 1) are summed in fp16
-            // pairs, then scaled by the block scale and max|x| in fp32
+            // pairs, scaled by the block scale into fp32 pair sums, and the
+            // row's sum by max|x| at the end
             float xsc[NE];  // per-token max|x|
 #pragma unroll
             for (int r = 0; r < NE; ++r) xsc[r] = (NE <= 2 || r < seg.n_e) ? xscale[seg.tok[r]] : 0.f;
@@ -299,10 +300,15 @@ __device__ __forceinline__ void gu_stage(const Args &a, const LayerW &lw, const 
                             pu1 = __hfma2(uh[q + 1], *reinterpret_cast<const __half2 *>(&xw[q + 1]), pu1);
                         }
                         const float2 fg = __half22float2(__hadd2(pg0, pg1)), fu = __half22float2(__hadd2(pu0, pu1));
-                        ag[r].x = fmaf(fg.x + fg.y, sgb * xsc[r], ag[r].x);
-                        au[r].x = fmaf(fu.x + fu.y, sub * xsc[r], au[r].x);
+                        ag[r] = ffma2(fg, make_float2(sgb, sgb), ag[r]);
+                        au[r] = ffma2(fu, make_float2(sub, sub), au[r]);
                     }
                 }
+            }
+#pragma unroll
+            for (int r = 0; r < NE; ++r) {
+                ag[r] = make_float2((ag[r].x + ag[r].y) * xsc[r], 0.f);
+                au[r] = make_float2((au[r].x + au[r].y) * xsc[r], 0.f);
             }
         } else
         for (int bb = lane; bb < d / 16; bb += 32) {
