@@ -112,13 +112,15 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.22e6 + 3.52e6,
+    "decode_t1": {"bytes": 304.21e6 + 3.24e6,
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_fused.cu",
-                              "top_moe_expert_router_gb300/csrc/common.cuh"),
-                  "sha256": ("6d828c4220d259f61ae9b2d532b6178dadd6062a79eafbf6cc60c4a174d426cb",
+                              "top_moe_expert_router_gb300/csrc/common.cuh",
+                              "top_moe_expert_router_gb300/csrc/decode_common.cuh"),
+                  "sha256": ("a80a6f64b0b32105cb76a5aa9281782345595ad3d125e6f211a678a6e9cc8960",
                              "1d39e048978fb78a6191116a4ce545b150e1efd7577999126a1f97db51c5e355",
-                             "7dd70629dc137bc914f03f15ee8566d22afb9a3e9583266dc02b5c21e57e759f")},
+                             "1e4bae8433f4bd55832d6ff4c6cc33eb01e10da95441e7ecae209f1d2717eec4",
+                             "a21051bb71d6311f1049221a1407b8a695c41fd4744e878851687f170279d32f")},
 }
 
 
