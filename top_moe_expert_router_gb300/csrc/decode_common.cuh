@@ -299,11 +299,64 @@ __device__ __forceinline__ void topk_sorted(uint32_t key[8], int k, int32_t *ids
 //     token counts, n_uniq + 1 entries);
 //  4. one thread per (token, pick) places it: experts ascending, tokens
 //     ascending within an expert.
-// Ends with __syncthreads().
+// One token skips 2.-4.: warp 0 ranks its k distinct experts (ascending,
+// they are its k rows) and fills R.cnt / R.off only with `counts` (otherwise
+// expert uniq[u] is known to hold one token, at row u). Ends with
+// __syncthreads().
 __device__ __forceinline__ void route_tokens(const Route &R, const float *logits, const uint64_t *tlogits,
                                              uint32_t tag, int T, int k, int E, uint32_t *err,
-                                             volatile int *abort_flag) {
+                                             volatile int *abort_flag, bool counts = true) {
     const int tid = threadIdx.x, nthr = blockDim.x, warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+    if (T == 1) {
+        // one token: its k distinct experts, ascending, are its k rows (warp
+        // 0 alone; the per-expert counts and first rows only with `counts`,
+        // after the barrier, for the records CTA 0 publishes)
+        if (warp == 0) {
+            uint32_t key[8];
+            if (tlogits)
+                lane_keys_tagged(tlogits, E, tag, key, err, abort_flag);
+            else
+                lane_keys(logits, E, key);
+            topk_sorted(key, k, R.ids, R.w);
+            __syncwarp();
+            int idq[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) idq[q] = q < k ? R.ids[q] : 0x7FFFFFFF;
+            int my = 0x7FFFFFFF;
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+                if (q == lane) my = idq[q];
+            int rank = 0;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) rank += idq[q] < my;
+            if (lane < k) {
+                R.uniq[rank] = my;
+                R.scan[rank] = rank;
+                R.perm[rank] = 0;
+                R.pos[lane] = rank;
+            }
+            if (lane == 0) {
+                R.off[E] = k;
+                R.scan[k] = k;
+                *R.n_uniq = k;
+            }
+        }
+        __syncthreads();
+        if (counts) {
+            for (int e = tid; e < E; e += nthr) {
+                int c = 0, o = 0;
+                for (int q = 0; q < k; ++q) {
+                    const int id = R.ids[q];
+                    c += id == e;
+                    o += id < e;
+                }
+                R.cnt[e] = c;
+                R.off[e] = o;
+            }
+            __syncthreads();
+        }
+        return;
+    }
     for (int e = tid; e < 256; e += nthr) R.bm[e] = 0u;
     for (int t = warp; t < T; t += nwarps) {
         uint32_t key[8];

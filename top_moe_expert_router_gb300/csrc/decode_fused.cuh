@@ -176,6 +176,15 @@ struct Seg {
 template <int TM>
 __device__ __forceinline__ void seg_load(Seg<TM> &s, const Route &R, int u) {
     s.u = u;
+    if (TM == 1) {
+        // one token (the routing leaves R.cnt / R.off to CTA 0): expert
+        // uniq[u] holds row u
+        s.e = R.uniq[u];
+        s.n_e = 1;
+        s.row0 = u;
+        s.tok[0] = 0;
+        return;
+    }
     s.e = R.uniq[u];
     s.n_e = R.cnt[s.e] < TM ? R.cnt[s.e] : TM;
     s.row0 = R.off[s.e];
@@ -502,6 +511,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     int *cb_todo = cb_rows_s + 32;                  // [32]
     int *n_todo = cb_todo + 32;
     float *xscale = reinterpret_cast<float *>(smem + 800);  // [16] NVFP4: per-token max|x|
+    Plan *plan1 = reinterpret_cast<Plan *>(smem + 896);     // one token: the plan, worked out during the routing
     float *part = reinterpret_cast<float *>(smem + 1024);   // [8 warps][TM] router partials
     unsigned char *rbase = smem + 2048;             // routing scratch (8 KB)
     Route R;
@@ -712,13 +722,18 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
         __syncthreads();
     }
 
+    // one token: its k experts are distinct, so the plan (equal shares of k
+    // experts' stages) does not wait for the routing; the producer warp,
+    // idle while warp 0 waits for the logits, works it out meanwhile
+    if (T == 1 && warp == kProducerWarp && lane == 0) *plan1 = make_plan(k, I, d / kDnRows, b, G);
     // ---- 2. routing, computed by every CTA in shared memory ----
     // (the logits come from every CTA's router: each word is waited for by
     // its tag, so no grid barrier stands between the router and the routing;
     // the test hook shifts the awaited tag to one that never comes)
     {
         const uint32_t hold = *reinterpret_cast<const volatile uint32_t *>(&ctrl->test_hold);
-        route_tokens(R, nullptr, a.ws.tlogits, ep0 + 1u + (uint32_t)layer + hold, T, k, E, err, abort_flag);
+        route_tokens(R, nullptr, a.ws.tlogits, ep0 + 1u + (uint32_t)layer + hold, T, k, E, err, abort_flag,
+                     b == 0 || T > 1);
     }
     const int n_uniq = *R.n_uniq;
     if (b == 0) publish_records(R, a.ws, T, k, E, n_uniq, kThreads);
@@ -735,7 +750,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
     // with more tokens cost more per stage; the shares are cut by weight.
     Plan pl;
     if (T == 1) {
-        pl = make_plan(n_uniq, I, d / kDnRows, b, G);
+        pl = *plan1;   // n_uniq == k
     } else {
         // the segments cut by weight: the eight cut points, one thread each
         int *cut = reinterpret_cast<int *>(R.wsum);   // free after the routing
