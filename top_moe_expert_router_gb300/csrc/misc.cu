@@ -15,37 +15,26 @@ namespace moe {
 // ---------------------------------------------------------------------------
 // combine: out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] )
 // ---------------------------------------------------------------------------
-// CPT consecutive expert outputs at Y + i, widened to fp32 (bf16 outputs:
-// one 16-byte load of 8; fp32 outputs: one 16-byte load of 4).
-template <int CPT>
-__device__ __forceinline__ void load_y(const float *Y, size_t i, float v[CPT]) {
-    static_assert(CPT == 4, "fp32 outputs: 4 columns per thread");
-    const float4 a = __ldcg(reinterpret_cast<const float4 *>(Y + i));
-    v[0] = a.x;
-    v[1] = a.y;
-    v[2] = a.z;
-    v[3] = a.w;
+// Column q of a 16-byte vector of expert outputs (bf16: 8 columns; fp32: 4).
+__device__ __forceinline__ float yelem(const uint4 &v, int q, const uint16_t *) {
+    const uint32_t w = q < 2 ? v.x : q < 4 ? v.y : q < 6 ? v.z : v.w;
+    return (q & 1) ? bf16hi(w) : bf16lo(w);
 }
-template <int CPT>
-__device__ __forceinline__ void load_y(const uint16_t *Y, size_t i, float v[CPT]) {
-    static_assert(CPT == 8, "bf16 outputs: 8 columns per thread");
-    const uint4 a = __ldcg(reinterpret_cast<const uint4 *>(Y + i));
-    const uint32_t w[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-        v[2 * q] = bf16lo(w[q]);
-        v[2 * q + 1] = bf16hi(w[q]);
-    }
+__device__ __forceinline__ float yelem(const uint4 &v, int q, const float *) {
+    return __uint_as_float(q == 0 ? v.x : q == 1 ? v.y : q == 2 ? v.z : v.w);
 }
 
 // out[t, c] = bf16( (res[t, c] +) sum_j w[t, j] * Y[pos[t, j], c] ), CPT
-// columns per thread; all slot records first, then all expert-output loads
-// (one 16-byte load per slot), then the sum in fp32, j ascending.
+// columns per thread (one 16-byte vector per slot); all slot records first,
+// then every load (the slots' outputs and the residual, kept packed until
+// used, so that four CTAs fit on an SM and hide the two dependent memory
+// latencies), then the sum in fp32, j ascending.
 template <typename YT, int CPT>
-__global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, const float *__restrict__ w,
-                                                      const int32_t *__restrict__ pos,
-                                                      const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
-                                                      int T, int d, int k, uint32_t *err, int rows) {
+__global__ void __launch_bounds__(256, 4) combine_kernel(const YT *__restrict__ Y, const float *__restrict__ w,
+                                                         const int32_t *__restrict__ pos,
+                                                         const uint16_t *__restrict__ res, uint16_t *__restrict__ out,
+                                                         int T, int d, int k, uint32_t *err, int rows) {
+    static_assert(CPT * sizeof(YT) == 16, "one 16-byte vector per slot");
     // launched as a programmatic dependent: Y, w and pos come from the
     // kernels before it
     asm volatile("griddepcontrol.wait;" ::: "memory");
@@ -64,14 +53,24 @@ __global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, 
             wj[j] = 0.f;
         }
     }
-    float y[8][CPT];
+    uint4 yv[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        if (j < k) {
-            load_y<CPT>(Y, (size_t)rj[j] * d + c, y[j]);
+    for (int j = 0; j < 8; ++j)
+        yv[j] = j < k ? __ldcg(reinterpret_cast<const uint4 *>(Y + (size_t)rj[j] * d + c)) : make_uint4(0, 0, 0, 0);
+    uint32_t rv[CPT / 2];
+#pragma unroll
+    for (int q = 0; q < CPT / 2; ++q) rv[q] = 0u;
+    if (res) {
+        if constexpr (CPT == 8) {
+            const uint4 r4 = *reinterpret_cast<const uint4 *>(res + (size_t)t * d + c);
+            rv[0] = r4.x;
+            rv[1] = r4.y;
+            rv[2] = r4.z;
+            rv[3] = r4.w;
         } else {
-#pragma unroll
-            for (int q = 0; q < CPT; ++q) y[j][q] = 0.f;
+            const uint2 r2 = *reinterpret_cast<const uint2 *>(res + (size_t)t * d + c);
+            rv[0] = r2.x;
+            rv[1] = r2.y;
         }
     }
     float acc[CPT];
@@ -81,21 +80,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const YT *__restrict__ Y, 
     for (int j = 0; j < 8; ++j)
         if (j < k) {
 #pragma unroll
-            for (int q = 0; q < CPT; ++q) acc[q] = fmaf(wj[j], y[j][q], acc[q]);
+            for (int q = 0; q < CPT; ++q) acc[q] = fmaf(wj[j], yelem(yv[j], q, Y), acc[q]);
         }
     if (res) {
 #pragma unroll
         for (int q = 0; q < CPT; q += 2) {
-            const uint32_t rv = *reinterpret_cast<const uint32_t *>(res + (size_t)t * d + c + q);
-            acc[q] += bf16lo(rv);
-            acc[q + 1] += bf16hi(rv);
+            acc[q] += bf16lo(rv[q / 2]);
+            acc[q + 1] += bf16hi(rv[q / 2]);
         }
     }
     uint32_t o[CPT / 2];
 #pragma unroll
     for (int q = 0; q < CPT / 2; ++q)
         o[q] = (uint32_t)f32_to_bf16_rn(acc[2 * q]) | ((uint32_t)f32_to_bf16_rn(acc[2 * q + 1]) << 16);
-    if (CPT == 8)
+    if constexpr (CPT == 8)
         *reinterpret_cast<uint4 *>(out + (size_t)t * d + c) = make_uint4(o[0], o[1], o[2], o[3]);
     else
         *reinterpret_cast<uint2 *>(out + (size_t)t * d + c) = make_uint2(o[0], o[1]);
