@@ -223,9 +223,28 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams &p, const TileInf
                 float *dst = p.out_f32 + (size_t)ti.ks * p.split_stride + orow * p.ld + col0;
                 if (EPI == EPI_LOGITS) {
                     const bool add_bias = p.bias && ti.ks == 0;  // once, with the first part of K
+                    if (col0 + 16 <= p.n_valid && (p.n_valid & 3) == 0 &&
+                        (!add_bias || (reinterpret_cast<uintptr_t>(p.bias) & 15u) == 0)) {
+                        // 16-byte stores: a lane's row is its own, so every
+                        // scalar store would be a separate L2 transaction
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (col0 + i < p.n_valid) dst[i] = __uint_as_float(v[i]) + (add_bias ? p.bias[col0 + i] : 0.f);
+                        for (int i = 0; i < 16; i += 4) {
+                            float4 o = make_float4(__uint_as_float(v[i]), __uint_as_float(v[i + 1]),
+                                                   __uint_as_float(v[i + 2]), __uint_as_float(v[i + 3]));
+                            if (add_bias) {
+                                const float4 bv = __ldg(reinterpret_cast<const float4 *>(p.bias + col0 + i));
+                                o.x += bv.x;
+                                o.y += bv.y;
+                                o.z += bv.z;
+                                o.w += bv.w;
+                            }
+                            *reinterpret_cast<float4 *>(dst + i) = o;
+                        }
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (col0 + i < p.n_valid) dst[i] = __uint_as_float(v[i]) + (add_bias ? p.bias[col0 + i] : 0.f);
+                    }
                 } else {
 #pragma unroll
                     for (int i = 0; i < 16; i += 4)
