@@ -344,21 +344,42 @@ cudaError_t launch_quantize_nvfp4(const uint16_t *W, int n, int rows, int K, uin
 // ---------------------------------------------------------------------------
 // gather: xperm[r, :] = x[perm[r], :] (prefill operand rows in expert order)
 // ---------------------------------------------------------------------------
-__global__ void gather_rows_kernel(const uint16_t *__restrict__ x, const int32_t *__restrict__ perm,
-                                   uint16_t *__restrict__ xp, int rows, int d, int T, uint32_t *err) {
-    const int r = blockIdx.x;
+// One warp per gathered row (8 rows per CTA): the row's token read once, then
+// all of the lane's 16-byte loads issued before its stores.
+__global__ void __launch_bounds__(256) gather_rows_kernel(const uint16_t *__restrict__ x,
+                                                          const int32_t *__restrict__ perm,
+                                                          uint16_t *__restrict__ xp, int rows, int d, int T,
+                                                          uint32_t *err) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;
     const int t = perm[r];
     if ((unsigned)t >= (unsigned)T) {
-        if (threadIdx.x == 0) atomicOr(err, ERRBIT_RANGE);
+        if (lane == 0) atomicOr(err, ERRBIT_RANGE);
         return;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
     uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = __ldg(src + i);
+    const int nv = d / 8;
+    constexpr int kV = 8;
+    for (int i0 = 0; i0 < nv; i0 += 32 * kV) {
+        uint4 v[kV];
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const int i = i0 + j * 32 + lane;
+            if (i < nv) v[j] = __ldg(src + i);
+        }
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const int i = i0 + j * 32 + lane;
+            if (i < nv) dst[i] = v[j];
+        }
+    }
 }
 
 cudaError_t launch_gather_rows(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T, cudaStream_t st) {
-    gather_rows_kernel<<<T * L.k, 256, 0, st>>>(x, ws.perm, ws.xperm, T * L.k, L.d, T, &ws.ctrl->err);
+    const int rows = T * L.k;
+    gather_rows_kernel<<<(rows + 7) / 8, 256, 0, st>>>(x, ws.perm, ws.xperm, rows, L.d, T, &ws.ctrl->err);
     return cudaGetLastError();
 }
 

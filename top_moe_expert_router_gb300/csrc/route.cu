@@ -10,6 +10,7 @@
 #include <math.h>
 
 #include "common.cuh"
+#include "decode_common.cuh"
 
 namespace moe {
 
@@ -251,7 +252,16 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, i
             if (e < E) s_row[warp][e] = l;
         }
         __syncwarp();
-        topk_warp(s_row[warp], E, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k, false);
+        {
+            // lane l takes experts 8l .. 8l+7 (the small-batch kernels' top-k)
+            uint32_t key[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int e = 8 * lane + i;
+                key[i] = e < E ? fused::expert_key(s_row[warp][e]) : 0u;
+            }
+            fused::topk_sorted(key, k, ws.ids + (size_t)t * k, ws.w + (size_t)t * k);
+        }
         __syncwarp();
         if (lane < k) {
             const int e = ws.ids[(size_t)t * k + lane];
@@ -272,9 +282,9 @@ __global__ void __launch_bounds__(256) route_chunk_kernel(int T, int k, int E, i
     if (!s_last) return;
     __threadfence();
     const int nch = gridDim.x;
-    // per-chunk counts are read 16 at a time, all loads of a batch issued
+    // per-chunk counts are read 64 at a time, all loads of a batch issued
     // before any use: one L2 round trip per batch, not per chunk
-    constexpr int kBatch = 16;
+    constexpr int kBatch = 64;
     for (int e = tid; e < E; e += 256) {
         int n = 0;
         for (int c0 = 0; c0 < nch; c0 += kBatch) {
