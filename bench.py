@@ -479,9 +479,18 @@ def measure_decode(ctx, w, gl, host):
     pool_np = token_pool(w, ctx.rank)
     pool = [ctx.bf(p) for p in pool_np]
     out = torch.empty((w.T, w.d), dtype=torch.bfloat16, device=ctx.device)
+    # One launch of ours per step (the launch list in profiles/ shows nothing
+    # else between the step events): the step's own events then time that
+    # kernel, and the library records no second pair of events inside the
+    # step (measured: that pair adds ~4 us to a 67 us step). With more
+    # launches per step the library's events time the layer kernel.
+    gl.forward(pool[0], out)
+    torch.cuda.synchronize()
+    single = gl.last_launch_count() == 1
     step_ms, clk, launches = timed_steps(ctx, lambda s: gl.forward(pool[s % POOL], out), args.steps, args.warmup,
-                                         gl.last_launch_count, lambda: gl.profile_begin(args.steps))
-    prof = gl.profile_end()
+                                         gl.last_launch_count,
+                                         None if single else (lambda: gl.profile_begin(args.steps)))
+    prof = step_ms.reshape(-1, 1) if single else gl.profile_end()
     assert gl.device_status() == 0, "device error"
     total_s = float(step_ms.sum()) / 1e3
     value, t_max = aggregate(w.T * args.steps, total_s, ctx.dist, ctx.device)
@@ -490,7 +499,10 @@ def measure_decode(ctx, w, gl, host):
     hbm = ctx.peaks["hbm_gbs"]
     k_ms = prof[:, 0].astype(np.float64)
     ach = float(layer_bytes.mean() / (k_ms.mean() / 1e3) / 1e9)
-    roof = {"kernel": "decode_layer_kernel", "bound": "hbm", "achieved": ach, "peak": hbm, "unit": "GB/s",
+    mma = args.decode_path == "tensor_cores" or (args.decode_path == "auto" and w.T >= 8)
+    roof = {"kernel": "decode_mma_kernel" if mma else "decode_layer_kernel", "bound": "hbm", "achieved": ach,
+            "peak": hbm, "unit": "GB/s", "timed_by": "step events (one launch per step)" if single else
+            "the library's events around the layer kernel",
             "frac": ach / hbm, "traffic": measured_traffic(w.name) if not args.experts else None,
             "peak_source": ctx.peak_src, "bytes_per_launch": float(layer_bytes.mean()),
             "bytes_rule": "unique active experts x 3*d*I*2 B + router E*d*2 B",
