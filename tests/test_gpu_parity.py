@@ -128,15 +128,17 @@ def test_chunked_path_for_shapes_the_gemms_do_not_take(gpu_lib):
 
 @pytest.mark.parametrize("path", ["cuda_cores", "tensor_cores"])
 def test_alternating_inputs_read_nothing_stale(gpu_lib, path):
-    """Successive forwards on one layer with different tokens: every result
-    matches the oracle. The workspace then always holds the previous call's
+    """Successive forwards on one layer with different tokens and token
+    counts (one token among them: its own routing path): every result matches
+    the oracle. The workspace then always holds the previous call's logits,
     token rows, h and expert outputs, so a hand-off that read them before the
-    current call rewrote them (a missing wait) shows up as a wrong token."""
+    current call rewrote them (a missing wait, a logit word taken with a stale
+    tag) shows up as a wrong token."""
     host = HostLayer(W["tiny"])
     gl = _gpu_layer(gpu_lib, host, max_tokens=16)
     gl.set_decode_path(gpu_lib.MOE_DECODE_CUDA_CORES if path == "cuda_cores" else gpu_lib.MOE_DECODE_TENSOR_CORES)
     L = host.oracle()
-    for i, T in enumerate([16, 16, 5, 16, 3, 16, 9, 16]):
+    for i, T in enumerate([16, 16, 5, 1, 16, 3, 1, 1, 16, 9, 2, 16]):
         x = datagen.tokens(host.w, T, start_row=3000 + 41 * i)
         y = gl.forward(to_dev_bf16(x))
         torch.cuda.synchronize()
