@@ -112,15 +112,15 @@ def aggregate(units_per_rank: float, seconds_per_rank: float, dist, device=None)
 # Valid only for the kernel source it was taken on: the sha256 of the kernel's
 # source files must match, else the bench reports traffic as null.
 TRAFFIC = {
-    "decode_t1": {"bytes": 304.23e6 + 3.10e6,
+    "decode_t1": {"bytes": 304.23e6 + 3.32e6,
                   "sources": ("top_moe_expert_router_gb300/csrc/decode_fused.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_fused.cu",
                               "top_moe_expert_router_gb300/csrc/common.cuh",
                               "top_moe_expert_router_gb300/csrc/decode_common.cuh"),
-                  "sha256": ("363057706e5c7e490b18c2f2d6a4bb040f6287735b75e83e8ef6af0c015c0b64",
+                  "sha256": ("dda2ca4a74c5a09ac6a1f90d0e72915d5cde06064ac2b6ae3d82ded3d5d41ef9",
                              "1d39e048978fb78a6191116a4ce545b150e1efd7577999126a1f97db51c5e355",
                              "1e4bae8433f4bd55832d6ff4c6cc33eb01e10da95441e7ecae209f1d2717eec4",
-                             "62e7d12d16836e7ae29c17150624eaf0495f305bb9c72a0659ab3b298b3dafec")},
+                             "dac14814856e90a1fc7b34e6b39a4cafaec2db008a714d6fe2cf1818f341f284")},
 }
 
 

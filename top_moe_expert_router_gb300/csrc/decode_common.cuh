@@ -11,6 +11,15 @@ namespace moe {
 
 namespace fused {
 
+// Stacked layers: the router rows of the next layer this CTA computes
+// (experts b, b + G), fetched into L2 while the current layer's weights
+// still stream, so that the next router reads them from L2, not HBM.
+__device__ __forceinline__ void prefetch_next_router(const LayerW &next, int b, int G, int E, int d) {
+    for (int e = b; e < E && e < b + 2 * G; e += G)
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(next.wr + (size_t)e * d), "r"((uint32_t)d * 2)
+                     : "memory");
+}
+
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t *p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");

@@ -848,6 +848,7 @@ __global__ void __launch_bounds__(Warps<TM, FP4>::kThreads, 1) decode_layer_kern
             }
         }
         __syncwarp();
+        if (STACK && layer + 1 < a.n_layers && lane == 0) prefetch_next_router(a.ws.stack[layer + 1], b, G, E, d);
         // every copy this lane issued must land before the CTA moves on (in a
         // normal run the consumers have waited for all of them already)
         if (lane < P) {

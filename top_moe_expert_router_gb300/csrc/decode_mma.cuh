@@ -479,6 +479,7 @@ __global__ void __launch_bounds__(Cfg<FP4>::kThreads, 1)
                         }
                     }
                 }
+                if (STACK && layer + 1 < a.n_layers) fused::prefetch_next_router(a.ws.stack[layer + 1], b, G, E, d);
             }
         } else if (warp == 1) {
             // -------------------------------- MMA issuer --------------------------------
