@@ -266,45 +266,68 @@ __global__ void __launch_bounds__(256) gather_rows_f16_kernel(const uint16_t *__
                                                               const int32_t *__restrict__ perm,
                                                               uint16_t *__restrict__ xp, float *__restrict__ rscale,
                                                               int rows, int d, int T, uint32_t *err) {
-    const int r = blockIdx.x;
+    // one warp per gathered row (8 rows per CTA): rows of up to 4096
+    // columns are held in registers (16 vectors per lane) between the max
+    // and the conversion; longer rows are read twice
+    constexpr int kV = 16;
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= rows) return;
     const int t = perm[r];
     if ((unsigned)t >= (unsigned)T) {
-        if (threadIdx.x == 0) atomicOr(err, ERRBIT_RANGE);
+        if (lane == 0) atomicOr(err, ERRBIT_RANGE);
         return;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(x + (size_t)t * d);
+    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * d);
+    const int nv = d / 8;
+    const bool held = nv <= 32 * kV;
+    uint4 v[kV];
     float m = 0.f;
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (held) {
 #pragma unroll
-        for (int j = 0; j < 4; ++j) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[j])), fabsf(bf16hi(w[j]))));
+        for (int j = 0; j < kV; ++j) {
+            const int i = lane + 32 * j;
+            v[j] = i < nv ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[q])), fabsf(bf16hi(w[q]))));
+        }
+    } else {
+        for (int i = lane; i < nv; i += 32) {
+            const uint4 a = __ldg(src + i);
+            const uint32_t w[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) m = fmaxf(m, fmaxf(fabsf(bf16lo(w[q])), fabsf(bf16hi(w[q]))));
+        }
     }
-    __shared__ float red[8];
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 16));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 8));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 4));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 2));
-    m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, 1));
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = m;
-    __syncthreads();
-    m = 0.f;
-    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) m = fmaxf(m, red[i]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
     int e = 0;
     if (m > 0.f) frexpf(m, &e);      // m = f * 2^e, f in [0.5, 1): 2^e >= m
     const float inv = ldexpf(1.f, -e);
-    if (threadIdx.x == 0) rscale[r] = ldexpf(1.f, e);
-    uint4 *dst = reinterpret_cast<uint4 *>(xp + (size_t)r * d);
-    for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
-        const uint4 v = __ldg(src + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    if (lane == 0) rscale[r] = ldexpf(1.f, e);
+    auto convert = [&](const uint4 &a) {
+        const uint32_t w[4] = {a.x, a.y, a.z, a.w};
         uint32_t o[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const __half2 h = __floats2half2_rn(bf16lo(w[j]) * inv, bf16hi(w[j]) * inv);
-            o[j] = *reinterpret_cast<const uint32_t *>(&h);
+        for (int q = 0; q < 4; ++q) {
+            const __half2 h = __floats2half2_rn(bf16lo(w[q]) * inv, bf16hi(w[q]) * inv);
+            o[q] = *reinterpret_cast<const uint32_t *>(&h);
         }
-        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+        return make_uint4(o[0], o[1], o[2], o[3]);
+    };
+    if (held) {
+#pragma unroll
+        for (int j = 0; j < kV; ++j) {
+            const int i = lane + 32 * j;
+            if (i < nv) dst[i] = convert(v[j]);
+        }
+    } else {
+        for (int i = lane; i < nv; i += 32) dst[i] = convert(__ldg(src + i));
     }
 }
 
@@ -324,8 +347,8 @@ static cudaError_t launch_fp4_gemm(const CUtensorMap &a, const CUtensorMap &q, c
 
 cudaError_t launch_gather_rows_f16(const LayerDev &L, const Workspace &ws, const uint16_t *x, int T,
                                    cudaStream_t st) {
-    fp4gemm::gather_rows_f16_kernel<<<T * L.k, 256, 0, st>>>(x, ws.perm, ws.xperm, ws.row_scale, T * L.k, L.d, T,
-                                                            &ws.ctrl->err);
+    fp4gemm::gather_rows_f16_kernel<<<(T * L.k + 7) / 8, 256, 0, st>>>(x, ws.perm, ws.xperm, ws.row_scale, T * L.k,
+                                                                      L.d, T, &ws.ctrl->err);
     return cudaGetLastError();
 }
 
